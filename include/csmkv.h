@@ -1,0 +1,205 @@
+/*
+ * csmkv.h -- C ABI of the GB300 (sm_103a) library for online KV-cache
+ * clustering: Chunked Soft Matching (CSM) compression and degree-aware
+ * ("log N") decode attention over the compressed cache.
+ *
+ * Defining sources (web pages on arXiv 2506.11418):
+ *   [Chelsea]    "Chelsea: Efficient Long-Context LLM Inference via KV Cache
+ *                Clustering" (xllm-io paper review): §三 核心公式 (attention with
+ *                cluster degrees), §三 算法流程 (Algorithm 1, the inference
+ *                pipeline), §三 分块软匹配算法 (CSM steps 1-4), §三 理论分析
+ *                (Theorem 6.1), §三 Outlier Heads处理.
+ *   [CentroidKV] "CentroidKV: Efficient Long-Context LLM Inference via KV Cache
+ *                Clustering" (gist.science explainer), 技术摘要: 推理流水线,
+ *                分块软匹配 (CSM) incl. 渐进式调度, 聚合.
+ *
+ * Conventions for every call below
+ *   - Memory: the caller owns every buffer. Device pointers must come from
+ *     device memory of the current CUDA device. The library never allocates.
+ *   - Cache layout (csmkv_cache): K and V are [batch][h_kv][cap][head_dim]
+ *     row-major in the cache dtype, N (cluster degrees) is int32
+ *     [batch][h_kv][cap], len is int32 [batch][h_kv] (rows in use per
+ *     (sequence, KV head)). A layer stack folds into batch. K, V, N bases must
+ *     be 16-byte aligned; cap must be a multiple of 8 and head_dim a multiple
+ *     of 8 with head_dim <= 128.
+ *   - Execution: every device call is asynchronous on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream). Nothing synchronises
+ *     the host and nothing reads device memory back, so calls can be issued
+ *     back to back or captured into a CUDA graph.
+ *   - Errors: argument errors return a csmkv_status synchronously without
+ *     launching anything. Errors found on the device (a full cache on append,
+ *     a bounded wait that ran out) are recorded, first one wins, in the status
+ *     word at offset 0 of the call's workspace; read it with
+ *     csmkv_device_status(), reset it with csmkv_clear_status(). A new
+ *     workspace must be zero-filled once before its first use. No kernel
+ *     traps or spins without bound.
+ *   - Workspaces: a workspace serves one call at a time; calls that share a
+ *     workspace must be ordered on one stream.
+ */
+#ifndef CSMKV_H
+#define CSMKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CSMKV_OK = 0,
+    CSMKV_ERR_ARG = 1,         /* an argument is out of its documented range */
+    CSMKV_ERR_DTYPE = 2,       /* unknown dtype */
+    CSMKV_ERR_ALIGN = 3,       /* a pointer or a size breaks the alignment rules */
+    CSMKV_ERR_CAPACITY = 4,    /* device: append into a cache with len == cap */
+    CSMKV_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the query says */
+    CSMKV_ERR_TIMEOUT = 6,     /* device: a bounded wait ran out; that work was skipped */
+    CSMKV_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+    CSMKV_ERR_UNSUPPORTED = 8  /* valid arguments no kernel here covers (e.g. h_q/h_kv > 8 on bf16) */
+} csmkv_status;
+
+typedef enum { CSMKV_BF16 = 0, CSMKV_F32 = 1 } csmkv_dtype;
+
+typedef struct {
+    int32_t batch;    /* independent sequences (times layers, when a stack is folded in) */
+    int32_t h_kv;     /* KV heads per sequence */
+    int32_t head_dim; /* d */
+    int32_t cap;      /* rows allocated per (sequence, KV head) */
+    int32_t dtype;    /* csmkv_dtype of K, V, q, k_new, v_new and the attention output */
+} csmkv_cache;
+
+/* ------------------------------------------------------------------------
+ * Chunked Soft Matching, one round   [Chelsea §三 分块软匹配算法 steps 1-4;
+ *                                     CentroidKV 分块软匹配 (CSM), 聚合]
+ *
+ * For every (sequence b, KV head h) with head_mask[h] == 0 and (seq_mask ==
+ * NULL or seq_mask[b] != 0), on its first s = len[b][h] rows:
+ *   - rows [0, n1) (attention sinks) and the last n2 rows (recent tokens) are
+ *     never merged; the middle [n1, s - n2) is cut into ch = floor((s-n1-n2)/c)
+ *     full chunks starting at row n1; a shorter remainder is left as it is;
+ *   - inside a chunk, A = even offsets, B = odd offsets (Theorem 6.1);
+ *   - each A token takes argmax_b cos(k_a, k_b) over the B tokens of its
+ *     chunk (keys only; cos = 0 for a zero key; ties -> lowest b);
+ *   - the m = floor(r*c + 1e-9) edges with the largest similarity are
+ *     selected (ties -> lowest a);
+ *   - every B token with selected edges becomes the degree-weighted mean of
+ *     itself and its A tokens, k = sum n_i k_i / sum n_i, likewise v,
+ *     n = sum n_i (pre-round values, fp32 arithmetic, rounded once to the
+ *     cache dtype); several A tokens may merge into one B;
+ *   - the selected A rows are removed and K, V, N are compacted in place in
+ *     original order (sinks, chunks, remainder, recent window);
+ *   - len[b][h] -= ch * m.
+ * Units that are masked, or have no full chunk, are untouched.
+ *
+ * K, V, N, len: device, in/out (layout above).
+ * n1, n2 >= 0; c even with 2 <= c <= 256; 0 <= r <= 0.5 (at most half of a
+ * chunk merges, as the pages state). r == 0 is a no-op.
+ * head_mask: device uint8 [h_kv], 1 = outlier head (left uncompressed), or
+ *   NULL (no outliers). The mask is a property of the layer's heads and is
+ *   shared by every sequence of the batch [Chelsea §三 Outlier Heads处理].
+ * seq_mask: device uint8 [batch], nonzero = compress this sequence in this
+ *   call, or NULL (all). Lets a ragged batch compress only the sequences
+ *   whose trigger fired.
+ * workspace: device, >= csm_workspace_bytes(cache, n1, n2, c) bytes,
+ *   zero-filled before its first use, not touched by anything else between
+ *   calls except csmkv_clear_status.
+ * bf16 with c == 256 and head_dim in {64, 128} runs the similarity tile on
+ * the tensor cores (tcgen05, fp32 accumulate); every other shape, and f32,
+ * runs it on fp32 CUDA cores.
+ * ---------------------------------------------------------------------- */
+size_t csm_workspace_bytes(const csmkv_cache* cache, int32_t n1, int32_t n2, int32_t c);
+
+int csm_compress(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+                 int32_t n1, int32_t n2, int32_t c, double r,
+                 const uint8_t* head_mask, const uint8_t* seq_mask,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Extra controls for csm_compress_ex. Zero-initialise for the defaults. */
+typedef struct {
+    int64_t wait_timeout_ns;  /* bound on each device-side wait; <= 0 -> 2 s */
+    int32_t withhold_signals; /* test hook: work items never publish their "loaded"
+                                 flags, so every wait on another item runs into the
+                                 timeout and reports CSMKV_ERR_TIMEOUT (the cache is
+                                 then partly compacted and must be discarded) */
+    int32_t force_simt;       /* 1 = use the CUDA-core similarity path everywhere */
+} csm_options;
+
+/* csm_compress plus two optional outputs/controls:
+ * match_out: device int32 [batch*h_kv][csm_max_chunks(...)][c/2] or NULL.
+ *   For every processed chunk j of unit u, entry [u][j][a] receives the B index
+ *   (0..c/2-1) that A token a merged into, or -1. Entries of chunks that were
+ *   not processed are left untouched.
+ * opts: NULL for defaults. */
+int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+                    int32_t n1, int32_t n2, int32_t c, double r,
+                    const uint8_t* head_mask, const uint8_t* seq_mask,
+                    int32_t* match_out, const csm_options* opts,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* Full chunks that fit in cap: max(0, (cap - n1 - n2) / c). */
+int32_t csm_max_chunks(const csmkv_cache* cache, int32_t n1, int32_t n2, int32_t c);
+
+/* ------------------------------------------------------------------------
+ * Decode append   [Chelsea §三 算法流程, Algorithm 1 decode update]
+ * K=[K,k], V=[V,v], N=[N,1], s=s+1 for every (sequence, KV head) whose
+ * sequence is selected (seq_mask NULL = all). k_new, v_new: device
+ * [batch][h_kv][head_dim] in the cache dtype. A unit with len == cap is left
+ * unchanged and CSMKV_ERR_CAPACITY is recorded in the workspace status word.
+ * workspace: device, >= csm_append_workspace_bytes() bytes (status only).
+ * ---------------------------------------------------------------------- */
+size_t csm_append_workspace_bytes(void);
+
+int csm_append(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+               const void* k_new, const void* v_new, const uint8_t* seq_mask,
+               void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Degree-aware decode attention   [Chelsea §三 核心公式; CentroidKV 聚合]
+ *   o_h = softmax(scale * q_h K^T + log N) V
+ *       = sum_t n_t exp(scale q_h.k_t) v_t / sum_t n_t exp(scale q_h.k_t)
+ * over the first len rows of KV head floor(h / G) of the same sequence,
+ * G = h_q / h_kv (contiguous query-head groups, GQA).
+ * q: device [batch][h_q][head_dim]; out: device [batch][h_q][head_dim], both
+ * in the cache dtype; K, V, N, len read only. A unit with len == 0 gives a
+ * zero output. scale is normally 1/sqrt(head_dim).
+ * h_q must be a positive multiple of h_kv; bf16 needs G <= 8 and head_dim in
+ * {64, 128} (CSMKV_ERR_UNSUPPORTED otherwise).
+ * workspace: device, >= decode_attn_workspace_bytes(cache, h_q) bytes.
+ * Work is split over the whole GPU by a flat partition of all units' tokens,
+ * so ragged lengths stay balanced; partial softmax states are combined by a
+ * second kernel.
+ * ---------------------------------------------------------------------- */
+size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t h_q);
+
+int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N,
+                     const int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale,
+                     void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host-side schedule helpers   [Chelsea §三 算法流程, Algorithm 1;
+ *                               CentroidKV 分块软匹配 (CSM), 渐进式调度]
+ * Pure functions; no device work.
+ * ---------------------------------------------------------------------- */
+double csm_budget(int64_t n, double R, int64_t Gamma);            /* B = R (n + Gamma) */
+int csm_should_trigger(int64_t s, double B, int32_t g);           /* s >= B + g */
+double csm_ratio(int32_t j, double r_init, double dr, double r_min); /* max(r_init - j dr, r_min) */
+int32_t csm_edges_per_chunk(double r, int32_t c);                 /* floor(r c + 1e-9) */
+int64_t csm_num_chunks(int64_t s, int32_t n1, int32_t n2, int32_t c); /* floor(max(0, s-n1-n2) / c) */
+int64_t csm_len_after(int64_t s, int32_t n1, int32_t n2, int32_t c, int32_t m); /* s - chunks * m */
+
+/* ------------------------------------------------------------------------
+ * Device status word (offset 0 of every workspace)
+ * ---------------------------------------------------------------------- */
+/* Synchronises `stream`, then returns the recorded csmkv_status (CSMKV_OK if
+ * none), or CSMKV_ERR_CUDA if the read itself failed. */
+int csmkv_device_status(const void* workspace, void* stream);
+/* Enqueues a reset of the status word to CSMKV_OK on `stream`. */
+int csmkv_clear_status(void* workspace, void* stream);
+/* Static description of a status code. */
+const char* csmkv_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSMKV_H */

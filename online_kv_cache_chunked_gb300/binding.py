@@ -1,0 +1,219 @@
+"""ctypes binding of the C ABI in include/csmkv.h (argument marshalling only).
+
+Every function here has the C name and forwards to libcsmkv.so; all the work
+of the path runs in its CUDA kernels. Tensors are torch CUDA tensors (device
+memory and streams come from PyTorch); the library itself never allocates.
+There is no CPU fallback: if the library is missing, load() raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+BF16, F32 = 0, 1
+_DTYPES = {torch.bfloat16: BF16, torch.float32: F32}
+
+STATUS = {0: "CSMKV_OK", 1: "CSMKV_ERR_ARG", 2: "CSMKV_ERR_DTYPE", 3: "CSMKV_ERR_ALIGN",
+          4: "CSMKV_ERR_CAPACITY", 5: "CSMKV_ERR_WORKSPACE", 6: "CSMKV_ERR_TIMEOUT",
+          7: "CSMKV_ERR_CUDA", 8: "CSMKV_ERR_UNSUPPORTED"}
+
+
+class CsmkvError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = int(code)
+        super().__init__(f"{fn}: {STATUS.get(self.code, self.code)} ({status_str(self.code)})")
+
+
+class Cache(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("h_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("cap", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class CsmOptions(ctypes.Structure):
+    _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("withhold_signals", ctypes.c_int32),
+                ("force_simt", ctypes.c_int32)]
+
+
+_lib = None
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int32
+I64 = ctypes.c_int64
+F64 = ctypes.c_double
+SZ = ctypes.c_size_t
+CP = ctypes.POINTER(Cache)
+
+_SIGS = {
+    "csm_workspace_bytes": (SZ, [CP, I32, I32, I32]),
+    "csm_compress": (ctypes.c_int, [P, P, P, P, CP, I32, I32, I32, F64, P, P, P, SZ, P]),
+    "csm_compress_ex": (ctypes.c_int, [P, P, P, P, CP, I32, I32, I32, F64, P, P, P,
+                                       ctypes.POINTER(CsmOptions), P, SZ, P]),
+    "csm_max_chunks": (I32, [CP, I32, I32, I32]),
+    "csm_append_workspace_bytes": (SZ, []),
+    "csm_append": (ctypes.c_int, [P, P, P, P, CP, P, P, P, P, SZ, P]),
+    "decode_attn_workspace_bytes": (SZ, [CP, I32]),
+    "decode_attn_logn": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
+    "csm_budget": (F64, [I64, F64, I64]),
+    "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
+    "csm_ratio": (F64, [I32, F64, F64, F64]),
+    "csm_edges_per_chunk": (I32, [F64, I32]),
+    "csm_num_chunks": (I64, [I64, I32, I32, I32]),
+    "csm_len_after": (I64, [I64, I32, I32, I32, I32]),
+    "csmkv_device_status": (ctypes.c_int, [P, P]),
+    "csmkv_clear_status": (ctypes.c_int, [P, P]),
+    "csmkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def library_path() -> str:
+    return _build.OUT
+
+
+def load():
+    """Loads libcsmkv.so (built by build()); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback path)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise CsmkvError(fn, rc)
+
+
+def cache_desc(K: torch.Tensor) -> Cache:
+    """Descriptor of a [batch, h_kv, cap, head_dim] cache tensor."""
+    if K.dim() != 4 or not K.is_contiguous():
+        raise ValueError("cache tensors are contiguous [batch, h_kv, cap, head_dim]")
+    if K.dtype not in _DTYPES:
+        raise ValueError(f"unsupported cache dtype {K.dtype}")
+    b, h, cap, d = K.shape
+    return Cache(b, h, d, cap, _DTYPES[K.dtype])
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace (allocated by PyTorch, not the library)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------- CSM
+def csm_workspace_bytes(cache: Cache, n1: int, n2: int, c: int) -> int:
+    return int(load().csm_workspace_bytes(ctypes.byref(cache), n1, n2, c))
+
+
+def csm_max_chunks(cache: Cache, n1: int, n2: int, c: int) -> int:
+    return int(load().csm_max_chunks(ctypes.byref(cache), n1, n2, c))
+
+
+def csm_compress(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, workspace=None,
+                 stream=None):
+    cache = cache_desc(K)
+    rc = load().csm_compress(_ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), n1, n2, c,
+                             float(r), _ptr(head_mask), _ptr(seq_mask), _ptr(workspace),
+                             workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("csm_compress", rc)
+
+
+def csm_compress_ex(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, match_out=None,
+                    wait_timeout_ns=0, withhold_signals=0, force_simt=0, workspace=None, stream=None):
+    cache = cache_desc(K)
+    opts = CsmOptions(int(wait_timeout_ns), int(withhold_signals), int(force_simt))
+    rc = load().csm_compress_ex(_ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), n1, n2, c,
+                                float(r), _ptr(head_mask), _ptr(seq_mask), _ptr(match_out),
+                                ctypes.byref(opts), _ptr(workspace),
+                                workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("csm_compress_ex", rc)
+
+
+# ---------------------------------------------------------------- append
+def csm_append_workspace_bytes() -> int:
+    return int(load().csm_append_workspace_bytes())
+
+
+def csm_append(K, V, N, length, k_new, v_new, seq_mask=None, workspace=None, stream=None):
+    cache = cache_desc(K)
+    rc = load().csm_append(_ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), _ptr(k_new),
+                           _ptr(v_new), _ptr(seq_mask), _ptr(workspace),
+                           workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("csm_append", rc)
+
+
+# ---------------------------------------------------------------- attention
+def decode_attn_workspace_bytes(cache: Cache, h_q: int) -> int:
+    return int(load().decode_attn_workspace_bytes(ctypes.byref(cache), h_q))
+
+
+def decode_attn_logn(q, K, V, N, length, out, workspace, scale=None, stream=None):
+    cache = cache_desc(K)
+    h_q = q.shape[1]
+    if scale is None:
+        scale = 1.0 / (K.shape[-1] ** 0.5)
+    rc = load().decode_attn_logn(_ptr(q), _ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), h_q,
+                                 float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("decode_attn_logn", rc)
+
+
+# ---------------------------------------------------------------- host helpers
+def csm_budget(n, R, Gamma) -> float:
+    return float(load().csm_budget(int(n), float(R), int(Gamma)))
+
+
+def csm_should_trigger(s, B, g) -> bool:
+    return bool(load().csm_should_trigger(int(s), float(B), int(g)))
+
+
+def csm_ratio(j, r_init, dr, r_min) -> float:
+    return float(load().csm_ratio(int(j), float(r_init), float(dr), float(r_min)))
+
+
+def csm_edges_per_chunk(r, c) -> int:
+    return int(load().csm_edges_per_chunk(float(r), int(c)))
+
+
+def csm_num_chunks(s, n1, n2, c) -> int:
+    return int(load().csm_num_chunks(int(s), int(n1), int(n2), int(c)))
+
+
+def csm_len_after(s, n1, n2, c, m) -> int:
+    return int(load().csm_len_after(int(s), int(n1), int(n2), int(c), int(m)))
+
+
+def csmkv_device_status(workspace, stream=None) -> int:
+    return int(load().csmkv_device_status(_ptr(workspace), _stream(stream)))
+
+
+def csmkv_clear_status(workspace, stream=None) -> None:
+    _check("csmkv_clear_status", load().csmkv_clear_status(_ptr(workspace), _stream(stream)))
+
+
+def status_str(code: int) -> str:
+    try:
+        return load().csmkv_status_str(int(code)).decode()
+    except Exception:  # the library may be missing while formatting an error
+        return "?"

@@ -1,0 +1,582 @@
+// decode_attn.cu -- degree-aware decode attention over a (compressed) KV cache.
+// [Chelsea §三 核心公式: O = softmax(q K^T / sqrt(d) + log N) V; CentroidKV 聚合]
+//
+// The log-degree bias is applied as a weight: e^(x + log n) = n e^x, so the
+// online softmax keeps (m, l, acc) with p_t = n_t * 2^(x_t - m), x_t the
+// base-2 scaled logit. No log is evaluated and integer degrees stay exact.
+//
+// Work split (bf16): all units' tokens are laid end to end and cut into one
+// equal range per CTA, so ragged lengths (outlier heads, ragged batches) stay
+// balanced over the whole GPU. A CTA walks its range unit by unit in 64-token
+// tiles: one producer warp streams K, V (128-byte swizzled, 2 boxes of 64
+// columns) and the degree tile into a 3-stage TMA/mbarrier ring; four consumer
+// warps each take 16 tokens of a tile and run S^T = K q^T and O^T += V^T P^T on
+// mma.sync (bf16 in, fp32 accumulate), the G <= 8 query heads of the group in
+// the N = 8 dimension, so each K/V byte is read once for the whole group. Each
+// warp writes one partial (m, l, acc) per unit it touched; a combine kernel
+// merges the partials of a unit into the output.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "host_util.h"
+#include "ptx.cuh"
+
+namespace csmkv {
+
+constexpr int kTile = 64;
+constexpr int kConsumerWarps = 4;
+constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kDecCtasPerSm = 2;
+constexpr int kSlotHeads = 8;  // partial records are padded to 8 heads
+
+struct DecParams {
+    const void* q;
+    const int32_t* len;
+    void* out;
+    WsHeader* hdr;
+    int32_t* prefix;      // [BH + 1] token offset of every unit
+    int32_t* cta_unit;    // [nCTA] first unit of every CTA's range (BH = none)
+    float* pm;            // [slots][8] running max (base-2 domain)
+    float* pl;            // [slots][8] running sum
+    float* pacc;          // [slots][8][D] unnormalised output
+    int32_t BH, Hkv, Hq, G, cap, D, nCTA;
+    float scale_log2;     // scale * log2(e)
+    float scale;          // natural-log scale (fp32 path)
+};
+
+// ----------------------------------------------------------------------------
+// Prologue (one CTA): prefix sums of the lengths, tokens per CTA, first unit of
+// every CTA's range.
+__global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p) {
+    __shared__ int wsum[32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < p.BH; base += 1024) {
+        const int u = base + tid;
+        int v = 0;
+        if (u < p.BH) {
+            v = p.len[u];
+            if (v < 0 || v > p.cap) {
+                record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                v = 0;
+            }
+        }
+        int incl = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += x;
+            }
+            wsum[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int carry = carry_s;
+        const int excl = carry + incl - v + (warp ? wsum[warp - 1] : 0);
+        if (u < p.BH) p.prefix[u] = excl;
+        __syncthreads();
+        if (tid == 1023) carry_s = excl + v;
+        __syncthreads();
+    }
+    const int total = carry_s;
+    if (tid == 0) p.prefix[p.BH] = total;
+    const int W = max(1, (total + p.nCTA - 1) / p.nCTA);
+    if (tid == 0) {
+        p.hdr->total_tokens = total;
+        p.hdr->tokens_per_cta = W;
+    }
+    __syncthreads();
+    for (int c = tid; c < p.nCTA; c += 1024) {
+        const long long start = (long long)c * W;
+        int lo = 0, hi = p.BH;  // first unit with prefix[u+1] > start
+        if (start >= total) {
+            lo = p.BH;
+        } else {
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (p.prefix[mid + 1] > start) hi = mid; else lo = mid + 1;
+            }
+        }
+        p.cta_unit[c] = lo;
+    }
+}
+
+// ----------------------------------------------------------------------------
+template <int D>
+struct DecGeom {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kBoxes * kBoxBytes;
+    static constexpr int kNOff = 2 * kBoxes * kBoxBytes;
+    static constexpr int kNBytes = (kTile + 4) * 4;            // 68 degrees (row rounded down to 4)
+    static constexpr int kStageBytes = kNOff + 1024;           // keeps stages 1024-aligned
+    static constexpr uint32_t kTxBytes = 2 * kBoxes * kBoxBytes + kNBytes;
+};
+
+// Walks a CTA's token range as (unit, first token, token count) segments.
+struct RangeWalker {
+    const int32_t* prefix;
+    int BH, u, tok, end;
+    __device__ bool next(int& unit, int& t0, int& n) {
+        while (u < BH && prefix[u + 1] <= tok) ++u;
+        if (tok >= end || u >= BH) return false;
+        const int seg_end = min(end, prefix[u + 1]);
+        unit = u;
+        t0 = tok - prefix[u];
+        n = seg_end - tok;
+        tok = seg_end;
+        return true;
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
+    decode_main_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN) {
+    using Geo = DecGeom<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* const sbase =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* const full = reinterpret_cast<uint64_t*>(sbase + kStages * Geo::kStageBytes);
+    uint64_t* const empty = full + kStages;
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int W = p.hdr->tokens_per_cta;
+    const int total = p.hdr->total_tokens;
+    const int r0 = blockIdx.x * W;
+    const int r1 = min(total, r0 + W);
+    if (r0 >= r1) return;
+    const int u0 = p.cta_unit[blockIdx.x];
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmN);
+    }
+    __syncthreads();
+    const uint64_t budget_ns = 2000000000ull;
+
+    if (warp == kConsumerWarps) {
+        // ============================================================ producer
+        int issued = 0;
+        if (lane == 0) {
+            RangeWalker rw{p.prefix, p.BH, u0, r0, r1};
+            int unit, t0, n;
+            bool ok = true;
+            while (ok && rw.next(unit, t0, n)) {
+                const long long row_base = (long long)unit * p.cap;
+                for (int t = 0; t < n && ok; t += kTile) {
+                    const int s = issued % kStages;
+                    if (issued >= kStages) {
+                        ok = mbar_wait(&empty[s], ((issued / kStages) - 1) & 1, globaltimer() + budget_ns);
+                        if (!ok || *abort_flag) { ok = false; break; }
+                    }
+                    const int row = (int)(row_base + t0 + t);
+                    uint8_t* st = sbase + s * Geo::kStageBytes;
+                    mbar_expect_tx(&full[s], Geo::kTxBytes);
+#pragma unroll
+                    for (int b = 0; b < Geo::kBoxes; ++b) {
+                        tma_load_2d(st + Geo::kKOff + b * Geo::kBoxBytes, &tmK, &full[s], b * 64, row);
+                        tma_load_2d(st + Geo::kVOff + b * Geo::kBoxBytes, &tmV, &full[s], b * 64, row);
+                    }
+                    tma_load_2d(st + Geo::kNOff, &tmN, &full[s], 0, row >> 2);
+                    ++issued;
+                }
+            }
+            if (!ok) {
+                record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // Drain: every issued stage must land before the CTA may exit.
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                (void)mbar_wait(&full[i % kStages], (i / kStages) & 1, globaltimer() + budget_ns);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ================================================================ consumers
+    const int g = lane >> 2, t4 = lane & 3;
+    const int tok_lo = warp * 16;
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
+    uint32_t qf[D / 16][2];
+    float oacc[D / 16][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    RangeWalker rw{p.prefix, p.BH, u0, r0, r1};
+    int unit, t0, n;
+    int consumed = 0;
+    bool ok = true;
+    while (ok && rw.next(unit, t0, n)) {
+        // query fragments of this unit's group: B[k = dim][n = head g]
+        const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
+        const __nv_bfloat16* qrow = qg + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            if (g < p.G) {
+                qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4);
+                qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * t4);
+            } else {
+                qf[ks][0] = 0u;
+                qf[ks][1] = 0u;
+            }
+        }
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) oacc[mb][0] = oacc[mb][1] = oacc[mb][2] = oacc[mb][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+        const long long row_base = (long long)unit * p.cap;
+
+        for (int t = 0; t < n; t += kTile) {
+            const int s = consumed % kStages;
+            ok = mbar_wait(&full[s], (consumed / kStages) & 1, globaltimer() + budget_ns);
+            if (!ok || *abort_flag) { ok = false; break; }
+            const int nv = min(kTile, n - t);  // valid tokens in this tile
+            uint8_t* st = sbase + s * Geo::kStageBytes;
+            const int noff = (int)((row_base + t0 + t) & 3);
+            const int* sN = reinterpret_cast<const int*>(st + Geo::kNOff) + noff;
+            if (tok_lo < nv) {
+                // ---- S^T = K q^T (16 tokens x 8 heads)
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int row = tok_lo + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int col = 16 * ks + (lane >> 4) * 8;
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(smem_u32(st + Geo::kKOff + (col >> 6) * Geo::kBoxBytes) + sw128_off(row, (col & 63) >> 3),
+                                a0, a1, a2, a3);
+                    mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                }
+                const int tA = tok_lo + g, tB = tA + 8;
+                const bool vA = tA < nv, vB = tB < nv;
+                const float x0 = vA ? sacc[0] * p.scale_log2 : -INFINITY;
+                const float x1 = vA ? sacc[1] * p.scale_log2 : -INFINITY;
+                const float x2 = vB ? sacc[2] * p.scale_log2 : -INFINITY;
+                const float x3 = vB ? sacc[3] * p.scale_log2 : -INFINITY;
+                float mh0 = fmaxf(x0, x2), mh1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, o));
+                    mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, o));
+                }
+                const float mn0 = fmaxf(m0, mh0), mn1 = fmaxf(m1, mh1);
+                const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+                const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+                const float nA = vA ? (float)sN[tA] : 0.f, nB = vB ? (float)sN[tB] : 0.f;
+                const float p0 = vA ? nA * exp2f(x0 - mn0) : 0.f;
+                const float p1 = vA ? nA * exp2f(x1 - mn1) : 0.f;
+                const float p2 = vB ? nB * exp2f(x2 - mn0) : 0.f;
+                const float p3 = vB ? nB * exp2f(x3 - mn1) : 0.f;
+                const uint32_t rowA = pack_bf16x2(p0, p1), rowB = pack_bf16x2(p2, p3);
+                // the denominator sums the same bf16-rounded weights the MMA sees
+                l0 = l0 * al0 + bf16lo(rowA) + bf16lo(rowB);
+                l1 = l1 * al1 + bf16hi(rowA) + bf16hi(rowB);
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                    for (int mb = 0; mb < D / 16; ++mb) {
+                        oacc[mb][0] *= al0;
+                        oacc[mb][1] *= al1;
+                        oacc[mb][2] *= al0;
+                        oacc[mb][3] *= al1;
+                    }
+                }
+                m0 = mn0;
+                m1 = mn1;
+                const uint32_t b0 = movmatrix_trans(rowA), b1 = movmatrix_trans(rowB);
+                if (tok_lo + 16 > nv) {
+                    // rows past the end may hold anything (NaN included): zero them so 0 * V stays 0
+                    for (int i = lane; i < 16 * 8 * Geo::kBoxes; i += 32) {
+                        const int r = tok_lo + i / (8 * Geo::kBoxes);
+                        const int rem = i % (8 * Geo::kBoxes);
+                        if (r >= nv)
+                            *reinterpret_cast<uint4*>(st + Geo::kVOff + (rem >> 3) * Geo::kBoxBytes + sw128_off(r, rem & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
+                // ---- O^T += V^T P^T (16 dims x 8 heads per m-block)
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) {
+                    const int row = tok_lo + (lane & 7) + (lane >> 4) * 8;
+                    const int col = 16 * mb + ((lane >> 3) & 1) * 8;
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(smem_u32(st + Geo::kVOff + (col >> 6) * Geo::kBoxBytes) + sw128_off(row, (col & 63) >> 3),
+                                      a0, a1, a2, a3);
+                    mma_bf16_16816(oacc[mb], a0, a1, a2, a3, b0, b1);
+                }
+                if (tok_lo + 16 > nv) fence_proxy_async_smem();  // generic zeroing before the next TMA into this stage
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++consumed;
+        }
+        if (!ok) break;
+        // ---- partial of (this CTA, this unit, this warp)
+        float lt0 = l0, lt1 = l1;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+            lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+        }
+        const size_t slot = ((size_t)blockIdx.x + unit) * kConsumerWarps + warp;
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        if (g == 0) {
+            if (h0 < p.G) { p.pm[slot * kSlotHeads + h0] = m0; p.pl[slot * kSlotHeads + h0] = lt0; }
+            if (h1 < p.G) { p.pm[slot * kSlotHeads + h1] = m1; p.pl[slot * kSlotHeads + h1] = lt1; }
+        }
+        float* acc0 = p.pacc + (slot * kSlotHeads + h0) * D;
+        float* acc1 = p.pacc + (slot * kSlotHeads + h1) * D;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            if (h0 < p.G) { acc0[16 * mb + g] = oacc[mb][0]; acc0[16 * mb + g + 8] = oacc[mb][2]; }
+            if (h1 < p.G) { acc1[16 * mb + g] = oacc[mb][1]; acc1[16 * mb + g + 8] = oacc[mb][3]; }
+        }
+    }
+    if (!ok) {
+        if (lane == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
+        *abort_flag = 1;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Combine: one warp per (unit, query head of the group).
+template <typename T>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecParams p) {
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.BH * p.G) return;
+    const int unit = gw / p.G, gh = gw - unit * p.G;
+    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
+    T* out = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G + gh) * p.D;
+    const int beg = p.prefix[unit], end = p.prefix[unit + 1];
+    if (end <= beg) {
+        for (int d = lane; d < p.D; d += 32) out[d] = T(0.f);
+        return;
+    }
+    const int W = p.hdr->tokens_per_cta;
+    const int c0 = beg / W, c1 = (end - 1) / W;
+    float M = -INFINITY;
+    for (int c = c0; c <= c1; ++c)
+        for (int w = 0; w < kConsumerWarps; ++w)
+            M = fmaxf(M, p.pm[(((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + gh]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
+    for (int c = c0; c <= c1; ++c)
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const size_t rec = (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + gh;
+            const float mw = p.pm[rec];
+            if (mw == -INFINITY) continue;
+            const float f = exp2f(mw - M);
+            L = fmaf(f, p.pl[rec], L);
+            const float* a = p.pacc + rec * p.D;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d = lane + 32 * i;
+                if (d < p.D) acc[i] = fmaf(f, a[d], acc[i]);
+            }
+        }
+    const float inv = 1.0f / L;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int d = lane + 32 * i;
+        if (d < p.D) out[d] = T(acc[i] * inv);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// fp32 path (exactness first): one CTA per (sequence, query head), four warps
+// over the tokens, lanes over the head dimension, fp32 online softmax.
+__global__ void __launch_bounds__(128) decode_f32_kernel(const DecParams p, const float* K, const float* V,
+                                                         const int32_t* N) {
+    const int bh = blockIdx.x;  // b * Hq + h
+    const int b = bh / p.Hq, h = bh - b * p.Hq, kv = h / p.G;
+    const int unit = b * p.Hkv + kv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = p.D;
+    int s = p.len[unit];
+    if (s < 0 || s > p.cap) {
+        if (threadIdx.x == 0) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+        s = 0;
+    }
+    const float* q = static_cast<const float*>(p.q) + (size_t)bh * D;
+    float qv[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qv[i] = (lane + 32 * i < D) ? q[lane + 32 * i] : 0.f;
+    float m = -INFINITY, l = 0.f;
+    const size_t base = (size_t)unit * p.cap;
+    for (int t = warp; t < s; t += 4) {
+        const float* k = K + (base + t) * D;
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (lane + 32 * i < D) dot = fmaf(qv[i], k[lane + 32 * i], dot);
+        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        const float x = dot * p.scale;
+        const float mn = fmaxf(m, x);
+        const float al = expf(m - mn);  // m = -inf on the first token -> 0
+        const float w = (float)N[base + t] * expf(x - mn);
+        l = l * al + w;
+        const float* v = V + (base + t) * D;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (lane + 32 * i < D) acc[i] = fmaf(w, v[lane + 32 * i], acc[i] * al);
+        m = mn;
+    }
+    __shared__ float sm[4], sl[4], sacc[4][128];
+    if (lane == 0) { sm[warp] = m; sl[warp] = l; }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (lane + 32 * i < D) sacc[warp][lane + 32 * i] = acc[i];
+    __syncthreads();
+    if (warp == 0) {
+        float M = fmaxf(fmaxf(sm[0], sm[1]), fmaxf(sm[2], sm[3]));
+        float L = 0.f, f[4];
+        for (int w = 0; w < 4; ++w) {
+            f[w] = (sm[w] == -INFINITY) ? 0.f : expf(sm[w] - M);
+            L += f[w] * sl[w];
+        }
+        float* out = static_cast<float*>(p.out) + (size_t)bh * D;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d = lane + 32 * i;
+            if (d < D) {
+                float a = 0.f;
+                for (int w = 0; w < 4; ++w) a = fmaf(f[w], sacc[w][d], a);
+                out[d] = (s > 0) ? a / L : 0.f;
+            }
+        }
+    }
+}
+
+static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, size_t* o_cta, size_t* o_pm,
+                         size_t* o_pl, size_t* o_pacc) {
+    const size_t BH = (size_t)cache->batch * cache->h_kv;
+    const size_t slots = ((size_t)nCTA + BH) * kConsumerWarps;
+    size_t off = kHeaderBytes;
+    *o_prefix = off;
+    off = align_up(off + (BH + 1) * 4, 256);
+    *o_cta = off;
+    off = align_up(off + (size_t)nCTA * 4, 256);
+    *o_pm = off;
+    off = align_up(off + slots * kSlotHeads * 4, 256);
+    *o_pl = off;
+    off = align_up(off + slots * kSlotHeads * 4, 256);
+    *o_pacc = off;
+    off = align_up(off + slots * kSlotHeads * (size_t)cache->head_dim * 4, 256);
+    return off;
+}
+
+template <int D>
+static int launch_decode_bf16(const DecParams& P, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tn, cudaStream_t st) {
+    constexpr int smem = kStages * DecGeom<D>::kStageBytes + 2 * kStages * 8 + 16 + 1024;
+    auto kern = decode_main_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return CSMKV_ERR_CUDA;
+    kern<<<P.nCTA, kDecThreads, smem, st>>>(P, tk, tv, tn);
+    return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
+}
+
+}  // namespace csmkv
+
+using namespace csmkv;
+
+extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t h_q) {
+    if (check_cache(cache) != CSMKV_OK || h_q < 1) return 0;
+    const int nCTA = sm_count() * kDecCtasPerSm;
+    if (nCTA <= 0) return 0;
+    size_t a, b, c, d, e;
+    return dec_layout(cache, nCTA, &a, &b, &c, &d, &e);
+}
+
+extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                                const csmkv_cache* cache, int32_t h_q, float scale, void* out, void* workspace,
+                                size_t ws_bytes, void* stream) {
+    int rc = check_cache(cache);
+    if (rc != CSMKV_OK) return rc;
+    if (!q || !K || !V || !N || !len || !out) return CSMKV_ERR_ARG;
+    if (h_q < 1 || (h_q % cache->h_kv) != 0) return CSMKV_ERR_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return CSMKV_ERR_ARG;
+    if (!aligned16(K) || !aligned16(V) || !aligned16(N) || !aligned16(q) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(len) & 3u))
+        return CSMKV_ERR_ALIGN;
+    const int G = h_q / cache->h_kv;
+    const int D = cache->head_dim;
+    const bool bf16 = cache->dtype == CSMKV_BF16;
+    if (bf16 && (G > 8 || (D != 64 && D != 128))) return CSMKV_ERR_UNSUPPORTED;
+    const int nCTA = sm_count() * kDecCtasPerSm;
+    if (nCTA <= 0) return CSMKV_ERR_CUDA;
+    size_t o_prefix, o_cta, o_pm, o_pl, o_pacc;
+    const size_t need = dec_layout(cache, nCTA, &o_prefix, &o_cta, &o_pm, &o_pl, &o_pacc);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecParams P{};
+    P.q = q;
+    P.len = len;
+    P.out = out;
+    P.hdr = reinterpret_cast<WsHeader*>(ws);
+    P.prefix = reinterpret_cast<int32_t*>(ws + o_prefix);
+    P.cta_unit = reinterpret_cast<int32_t*>(ws + o_cta);
+    P.pm = reinterpret_cast<float*>(ws + o_pm);
+    P.pl = reinterpret_cast<float*>(ws + o_pl);
+    P.pacc = reinterpret_cast<float*>(ws + o_pacc);
+    P.BH = cache->batch * cache->h_kv;
+    P.Hkv = cache->h_kv;
+    P.Hq = h_q;
+    P.G = G;
+    P.cap = cache->cap;
+    P.D = D;
+    P.nCTA = nCTA;
+    P.scale = scale;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (!bf16) {
+        decode_f32_kernel<<<cache->batch * h_q, 128, 0, st>>>(P, static_cast<const float*>(K),
+                                                              static_cast<const float*>(V), N);
+        return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
+    }
+
+    const uint64_t rows = (uint64_t)cache->batch * cache->h_kv * cache->cap;
+    CUtensorMap tk{}, tv{}, tn{};
+    {
+        const uint64_t dims[2] = {(uint64_t)D, rows};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64, (uint32_t)kTile};
+        if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(K), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(V), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return CSMKV_ERR_CUDA;
+        const uint64_t ndims[2] = {4, rows / 4};
+        const uint64_t nstr[1] = {16};
+        const uint32_t nbox[2] = {4, (uint32_t)(kTile / 4 + 1)};
+        if (!encode_tiled(&tn, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t*>(N), ndims, nstr, nbox,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+            return CSMKV_ERR_CUDA;
+    }
+    decode_prologue_kernel<<<1, 1024, 0, st>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
+    rc = D == 128 ? launch_decode_bf16<128>(P, tk, tv, tn, st) : launch_decode_bf16<64>(P, tk, tv, tn, st);
+    if (rc != CSMKV_OK) return rc;
+    decode_combine_kernel<__nv_bfloat16><<<(P.BH * G + 7) / 8, 256, 0, st>>>(P);
+    return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
+}

@@ -1,0 +1,55 @@
+// host_util.h -- host-side helpers shared by the library's translation units:
+// tensor-map encoding (driver entry point fetched through the runtime, so the
+// library needs no -lcuda), per-device SM count, and argument checks.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/csmkv.h"
+
+namespace csmkv {
+
+constexpr size_t kHeaderBytes = 256;  // every workspace starts with this header
+
+// Layout of the workspace header (offset 0). Only `status` is part of the public contract.
+struct WsHeader {
+    int32_t status;       // first device-side error (csmkv_status), sticky
+    int32_t ticket;       // work-ticket counter of the current call
+    int32_t epoch;        // call sequence number; flags equal to it are "set"
+    int32_t levels_ch;    // CSM: max full chunks over active units
+    int32_t levels_tail;  // CSM: max tail pieces over active units
+    int32_t total_tokens; // decode: tokens over all units
+    int32_t tokens_per_cta;
+    int32_t pad[57];
+};
+static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t dtype_bytes(int32_t dt) { return dt == CSMKV_BF16 ? 2 : (dt == CSMKV_F32 ? 4 : 0); }
+
+// Validates the cache descriptor itself; returns CSMKV_OK or the error.
+inline int check_cache(const csmkv_cache* c) {
+    if (!c) return CSMKV_ERR_ARG;
+    if (c->dtype != CSMKV_BF16 && c->dtype != CSMKV_F32) return CSMKV_ERR_DTYPE;
+    if (c->batch < 1 || c->h_kv < 1 || c->cap < 8 || (c->cap % 8) != 0) return CSMKV_ERR_ARG;
+    if (c->head_dim < 8 || c->head_dim > 128 || (c->head_dim % 8) != 0) return CSMKV_ERR_ARG;
+    const long long rows = (long long)c->batch * c->h_kv * c->cap;
+    if (rows > 0x7FFFFFFFLL) return CSMKV_ERR_ARG;  // row coordinates are int32
+    return CSMKV_OK;
+}
+
+int sm_count();                 // SMs of the current device (cached per device)
+const void* encode_fn();        // cuTensorMapEncodeTiled, or nullptr
+
+// Encodes a tiled tensor map; returns false on failure.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle);
+
+}  // namespace csmkv

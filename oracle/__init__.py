@@ -54,12 +54,12 @@ def _load():
         lib.oracle_partition.argtypes = [i32, P, P]
         lib.oracle_num_chunks.argtypes = [i32, i32, i32, i32]
         lib.oracle_num_chunks.restype = i32
-        lib.oracle_csm_chunk.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]
+        lib.oracle_csm_chunk.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_csm_chunk.restype = ctypes.c_int
         lib.oracle_csm_round.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
-                                         P, P, P, P, P, P, i32, i32]
+                                         P, P, P, P, P, P, i32, P, P, i32]
         lib.oracle_csm_round.restype = ctypes.c_int
-        lib.oracle_csm_chunks.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32]
+        lib.oracle_csm_chunks.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, i32]
         lib.oracle_csm_chunks.restype = ctypes.c_int
         lib.oracle_append.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
         lib.oracle_append.restype = i32
@@ -106,19 +106,22 @@ def csm_chunks(Kc, Vc, Nc, m: int, forced=None, nthreads=None):
     """CSM steps 2-7 on a list of independent chunks.
 
     Kc, Vc: [n, c, d]; Nc: [n, c]. Returns dict with K, V [n, c-m, d], N [n, c-m],
-    match/sim/margin [n, c/2] and cut [n].
+    match/sim/margin [n, c/2], cut [n] and origin/merged [n, c-m] (chunk offset
+    each output row comes from, and whether it is a merged centroid).
     """
     Kc, Vc, Nc = _f64(Kc), _f64(Vc), _i32(Nc)
     n, c, d = Kc.shape
     h = c // 2
     out = dict(K=np.zeros((n, c - m, d)), V=np.zeros((n, c - m, d)),
                N=np.zeros((n, c - m), np.int32), match=np.zeros((n, h), np.int32),
-               sim=np.zeros((n, h)), margin=np.zeros((n, h)), cut=np.zeros(n))
+               sim=np.zeros((n, h)), margin=np.zeros((n, h)), cut=np.zeros(n),
+               origin=np.zeros((n, c - m), np.int32), merged=np.zeros((n, c - m), np.uint8))
     f = None if forced is None else _i32(forced)
     rc = _load().oracle_csm_chunks(_ptr(Kc), _ptr(Vc), _ptr(Nc), n, c, d, m, _ptr(f),
                                    _ptr(out["K"]), _ptr(out["V"]), _ptr(out["N"]),
                                    _ptr(out["match"]), _ptr(out["sim"]), _ptr(out["margin"]),
-                                   _ptr(out["cut"]), _threads(nthreads))
+                                   _ptr(out["cut"]), _ptr(out["origin"]), _ptr(out["merged"]),
+                                   _threads(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_csm_chunks failed ({rc})")
     return out
@@ -128,21 +131,24 @@ def csm_round(K, V, N, length, n1: int, n2: int, c: int, m: int, skip=None,
               forced=None, nthreads=None):
     """One CSM round over BH caches. K, V: [BH, cap, d]; N: [BH, cap]; length: [BH].
 
-    Inputs are not modified. Returns dict with the new K, V, N, len and the
+    Inputs are not modified. Returns dict with the new K, V, N, len, the
     per-chunk records match/sim/margin [BH, maxch, c/2] and cut [BH, maxch]
-    (maxch = chunks that fit in cap).
+    (maxch = chunks that fit in cap), and per output row its pre-round row
+    (origin [BH, cap]) and whether it is a merged centroid (merged [BH, cap]).
     """
     K, V, N, L = _f64(K).copy(), _f64(V).copy(), _i32(N).copy(), _i32(length).copy()
     BH, cap, d = K.shape
     h = c // 2
     maxch = max(1, (cap - n1 - n2) // c)
     rec = dict(match=np.full((BH, maxch, h), -1, np.int32), sim=np.zeros((BH, maxch, h)),
-               margin=np.zeros((BH, maxch, h)), cut=np.zeros((BH, maxch)))
+               margin=np.zeros((BH, maxch, h)), cut=np.zeros((BH, maxch)),
+               origin=np.zeros((BH, cap), np.int32), merged=np.zeros((BH, cap), np.uint8))
     sk = None if skip is None else np.ascontiguousarray(np.asarray(skip, dtype=np.uint8))
     f = None if forced is None else _i32(forced)
     rc = _load().oracle_csm_round(_ptr(K), _ptr(V), _ptr(N), _ptr(L), BH, cap, d, n1, n2, c, m,
                                   _ptr(sk), _ptr(f), _ptr(rec["match"]), _ptr(rec["sim"]),
-                                  _ptr(rec["margin"]), _ptr(rec["cut"]), maxch, _threads(nthreads))
+                                  _ptr(rec["margin"]), _ptr(rec["cut"]), maxch, _ptr(rec["origin"]),
+                                  _ptr(rec["merged"]), _threads(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_csm_round failed ({rc})")
     return dict(K=K, V=V, N=N, len=L, **rec)

@@ -89,13 +89,15 @@ static int edge_cmp(const void* p, const void* q)
  * *cut_margin = (m-th largest edge sim) - ((m+1)-th), +inf when undefined.
  * forced (may be NULL): decisions to apply instead of steps 4-5 (the replay
  * used when the GPU took a near-tie the other way); similarities are still
- * reported. Returns 0, or -1 if forced does not hold exactly m edges or
- * points outside B.
+ * reported. origin/merged (may be NULL): per output row, the chunk offset it
+ * comes from and whether it is a merged centroid (bookkeeping for tests).
+ * Returns 0, or -1 if forced does not hold exactly m edges or points outside B.
  */
 int oracle_csm_chunk(const double* Kc, const double* Vc, const int32_t* Nc,
                      int32_t c, int32_t d, int32_t m, const int32_t* forced,
                      double* Ko, double* Vo, int32_t* No, int32_t* match,
-                     double* best_sim, double* margin, double* cut_margin)
+                     double* best_sim, double* margin, double* cut_margin,
+                     int32_t* origin, uint8_t* merged)
 {
     const int32_t h = c / 2;
     int32_t* best = (int32_t*)malloc(sizeof(int32_t) * h);
@@ -150,12 +152,16 @@ int oracle_csm_chunk(const double* Kc, const double* Vc, const int32_t* Nc,
             memcpy(Ko + (size_t)out * d, Kc + (size_t)o * d, sizeof(double) * d);
             memcpy(Vo + (size_t)out * d, Vc + (size_t)o * d, sizeof(double) * d);
             No[out] = Nc[o];
+            if (origin) origin[out] = o;
+            if (merged) merged[out] = 0;
             ++out;
             continue;
         }
         const int32_t b = o / 2;
         int incoming = 0;
         for (int32_t a = 0; a < h; ++a) incoming |= (match[a] == b);
+        if (origin) origin[out] = o;
+        if (merged) merged[out] = (uint8_t)(incoming != 0);
         if (!incoming) { /* a singleton keeps its exact values */
             memcpy(Ko + (size_t)out * d, Kc + (size_t)o * d, sizeof(double) * d);
             memcpy(Vo + (size_t)out * d, Vc + (size_t)o * d, sizeof(double) * d);
@@ -207,8 +213,15 @@ int32_t oracle_num_chunks(int32_t s, int32_t n1, int32_t n2, int32_t c)
 static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
                     int32_t d, int32_t n1, int32_t n2, int32_t c, int32_t m,
                     const int32_t* forced, int32_t* match, double* sim,
-                    double* margin, double* cut, int32_t maxch)
+                    double* margin, double* cut, int32_t maxch,
+                    int32_t* origin, uint8_t* merged)
 {
+    /* origin/merged (may be NULL): [cap], per output row the pre-round row it
+     * comes from and whether it is a merged centroid; identity when nothing merges */
+    if (origin)
+        for (int32_t t = 0; t < *len; ++t) origin[t] = t;
+    if (merged)
+        for (int32_t t = 0; t < *len; ++t) merged[t] = 0;
     const int32_t s = *len;
     const int32_t h = c / 2;
     const int32_t ch = oracle_num_chunks(s, n1, n2, c);
@@ -228,6 +241,8 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
     int32_t* mt = (int32_t*)malloc(sizeof(int32_t) * h);
     double* bs = (double*)malloc(sizeof(double) * h);
     double* mg = (double*)malloc(sizeof(double) * h);
+    int32_t* og = (int32_t*)malloc(sizeof(int32_t) * c);
+    uint8_t* mf = (uint8_t*)malloc((size_t)c);
     int rc = 0;
     int32_t w = start; /* next output row */
     for (int32_t j = 0; j < ch && rc == 0; ++j) {
@@ -235,7 +250,12 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
         const size_t base = (size_t)j * c;
         rc = oracle_csm_chunk(K0 + base * d, V0 + base * d, N0 + base, c, d, m,
                               forced ? forced + (size_t)j * h : NULL,
-                              K + (size_t)w * d, V + (size_t)w * d, N + w, mt, bs, mg, &cm);
+                              K + (size_t)w * d, V + (size_t)w * d, N + w, mt, bs, mg, &cm,
+                              og, mf);
+        for (int32_t o = 0; o < c - m; ++o) {
+            if (origin) origin[w + o] = start + j * c + og[o];
+            if (merged) merged[w + o] = mf[o];
+        }
         if (match) memcpy(match + (size_t)j * h, mt, sizeof(int32_t) * h);
         if (sim) memcpy(sim + (size_t)j * h, bs, sizeof(double) * h);
         if (margin) memcpy(margin + (size_t)j * h, mg, sizeof(double) * h);
@@ -249,6 +269,10 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
         memcpy(K + (size_t)w * d, K0 + (size_t)tail0 * d, sizeof(double) * (size_t)tail * d);
         memcpy(V + (size_t)w * d, V0 + (size_t)tail0 * d, sizeof(double) * (size_t)tail * d);
         memcpy(N + w, N0 + tail0, sizeof(int32_t) * (size_t)tail);
+        for (int32_t t = 0; t < tail; ++t) {
+            if (origin) origin[w + t] = start + tail0 + t;
+            if (merged) merged[w + t] = 0;
+        }
         *len = s - ch * m;
     }
     free(K0);
@@ -257,6 +281,8 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
     free(mt);
     free(bs);
     free(mg);
+    free(og);
+    free(mf);
     (void)cap;
     return rc;
 }
@@ -265,15 +291,16 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
  * One CSM round over BH = batch * h_kv independent caches.
  * K, V: [BH][cap][d] fp64; N: [BH][cap]; len: [BH]. skip[u] != 0 leaves unit
  * u untouched (outlier head, or a sequence not compressed this round).
- * Records: match/sim/margin [BH][maxch][c/2], cut [BH][maxch], all optional;
- * forced [BH][maxch][c/2] optional. Returns 0 on success, else the first
+ * Records: match/sim/margin [BH][maxch][c/2], cut [BH][maxch], origin and
+ * merged [BH][cap], all optional; forced [BH][maxch][c/2] optional. Returns 0 on success, else the first
  * failing unit's code (-1 bad forced decisions, -2 maxch too small).
  */
 int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
                      int32_t BH, int32_t cap, int32_t d, int32_t n1, int32_t n2,
                      int32_t c, int32_t m, const uint8_t* skip,
                      const int32_t* forced, int32_t* match, double* sim,
-                     double* margin, double* cut, int32_t maxch, int32_t nthreads)
+                     double* margin, double* cut, int32_t maxch,
+                     int32_t* origin, uint8_t* merged, int32_t nthreads)
 {
     int rc_all = 0;
     const size_t rec = (size_t)maxch * (c / 2);
@@ -286,7 +313,9 @@ int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
                           match ? match + u * rec : NULL,
                           sim ? sim + u * rec : NULL,
                           margin ? margin + u * rec : NULL,
-                          cut ? cut + (size_t)u * maxch : NULL, maxch);
+                          cut ? cut + (size_t)u * maxch : NULL, maxch,
+                          origin ? origin + (size_t)u * cap : NULL,
+                          merged ? merged + (size_t)u * cap : NULL);
         if (rc != 0) {
 #pragma omp critical
             if (rc_all == 0) rc_all = rc;
@@ -298,13 +327,14 @@ int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
 /*
  * A list of independent chunks (pre-round values), as used for sampled checks
  * at full size. Kc, Vc: [n][c][d]; Nc: [n][c]. Outputs: Ko, Vo [n][c-m][d],
- * No [n][c-m]; match/sim/margin [n][c/2]; cut [n]. forced optional [n][c/2].
+ * No [n][c-m]; match/sim/margin [n][c/2]; cut [n]; origin/merged [n][c-m].
+ * forced optional [n][c/2].
  */
 int oracle_csm_chunks(const double* Kc, const double* Vc, const int32_t* Nc,
                       int32_t n, int32_t c, int32_t d, int32_t m,
                       const int32_t* forced, double* Ko, double* Vo, int32_t* No,
                       int32_t* match, double* sim, double* margin, double* cut,
-                      int32_t nthreads)
+                      int32_t* origin, uint8_t* merged, int32_t nthreads)
 {
     int rc_all = 0;
     const int32_t h = c / 2;
@@ -315,7 +345,8 @@ int oracle_csm_chunks(const double* Kc, const double* Vc, const int32_t* Nc,
                                   forced ? forced + (size_t)i * h : NULL,
                                   Ko + (size_t)i * (c - m) * d, Vo + (size_t)i * (c - m) * d,
                                   No + (size_t)i * (c - m), match + (size_t)i * h,
-                                  sim + (size_t)i * h, margin + (size_t)i * h, cut + i);
+                                  sim + (size_t)i * h, margin + (size_t)i * h, cut + i,
+                                  origin + (size_t)i * (c - m), merged + (size_t)i * (c - m));
         if (rc != 0) {
 #pragma omp critical
             if (rc_all == 0) rc_all = rc;

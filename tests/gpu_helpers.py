@@ -1,0 +1,86 @@
+"""Helpers for the GPU parity tests: run a CSM round through the C ABI and judge it
+against the oracle with the rules in oracle/compare.py."""
+import numpy as np
+import torch
+
+import oracle
+from oracle import compare
+from online_kv_cache_chunked_gb300 import binding as B
+
+
+def to64(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def snapshot(K, V, N, L):
+    BH = K.shape[0] * K.shape[1]
+    cap, d = K.shape[2], K.shape[3]
+    return dict(K=to64(K).reshape(BH, cap, d), V=to64(V).reshape(BH, cap, d),
+                N=N.cpu().numpy().reshape(BH, cap).copy(), len=L.cpu().numpy().reshape(BH).copy())
+
+
+def skip_vector(batch, h_kv, head_mask=None, seq_mask=None):
+    sk = np.zeros(batch * h_kv, np.uint8)
+    for u in range(batch * h_kv):
+        b, h = divmod(u, h_kv)
+        if head_mask is not None and int(head_mask[h]):
+            sk[u] = 1
+        if seq_mask is not None and not int(seq_mask[b]):
+            sk[u] = 1
+    return sk
+
+
+def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, force_simt=0, ws=None):
+    cache = B.cache_desc(K)
+    maxch = max(1, B.csm_max_chunks(cache, n1, n2, c))
+    match = torch.full((K.shape[0] * K.shape[1], maxch, c // 2), -2, dtype=torch.int32, device=K.device)
+    if ws is None:
+        ws = B.new_workspace(B.csm_workspace_bytes(cache, n1, n2, c), K.device)
+    hm = None if head_mask is None else torch.as_tensor(np.asarray(head_mask, np.uint8)).to(K.device)
+    sm = None if seq_mask is None else torch.as_tensor(np.asarray(seq_mask, np.uint8)).to(K.device)
+    B.csm_compress_ex(K, V, N, L, n1, n2, c, r, head_mask=hm, seq_mask=sm, match_out=match,
+                      force_simt=force_simt, workspace=ws)
+    torch.cuda.synchronize()
+    st = B.csmkv_device_status(ws)
+    assert st == 0, f"device status {st}: {B.status_str(st)}"
+    return match.cpu().numpy()
+
+
+def round_parity(K, V, N, L, n1, n2, c, r, dtype, head_mask=None, seq_mask=None, force_simt=0, max_dev_frac=0.01):
+    """Runs one device round in place and checks it against the oracle. Returns stats."""
+    pre = snapshot(K, V, N, L)
+    m = B.csm_edges_per_chunk(r, c)
+    gm = gpu_round(K, V, N, L, n1, n2, c, r, head_mask, seq_mask, force_simt)
+    post = snapshot(K, V, N, L)
+    sk = skip_vector(K.shape[0], K.shape[1], head_mask, seq_mask)
+    free = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk)
+    n_chunks = np.array([0 if sk[u] else oracle.num_chunks(int(pre["len"][u]), n1, n2, c)
+                         for u in range(len(sk))])
+    if m == 0:
+        n_chunks[:] = 0
+    dev, fails = compare.check_round(pre["K"], free, gm, n_chunks, m, n1, c)
+    assert not fails, "\n".join(fails[:10])
+    forced = np.where(gm >= -1, gm, -1)
+    rep = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk, forced=forced)
+    fails, worst = compare.compare_state(rep, pre, post, dtype)
+    assert not fails, "\n".join(fails[:10])
+    # unprocessed units stay bit-identical
+    for u in np.nonzero(n_chunks == 0)[0]:
+        s = int(pre["len"][u])
+        assert int(post["len"][u]) == s
+        assert np.array_equal(post["K"][u, :s], pre["K"][u, :s])
+        assert np.array_equal(post["N"][u, :s], pre["N"][u, :s])
+    total = int(n_chunks.sum())
+    assert dev <= max(2, max_dev_frac * total), f"{dev} of {total} chunks deviate (near-ties)"
+    return dict(chunks=total, deviating=dev, worst_ratio=worst)
+
+
+def attn_parity(q, K, V, N, L, out, dtype, scale=None):
+    Bsz, Hkv = K.shape[0], K.shape[1]
+    ref = oracle.decode_attn_logn(to64(q), to64(K), to64(V), N.cpu().numpy(), L.cpu().numpy(), q.shape[1],
+                                  scale=scale)
+    got = to64(out)
+    err = float(np.abs(got - ref).max()) if got.size else 0.0
+    assert np.isfinite(got).all()
+    assert err <= compare.ATTN_TOL[dtype], f"attention max error {err}"
+    return err

@@ -1,0 +1,130 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every declared symbol,
+its host helpers agree with the oracle's schedule, and argument errors come back
+synchronously without touching a GPU."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import oracle
+from oracle import schedule as osched
+from online_kv_cache_chunked_gb300 import _build
+from online_kv_cache_chunked_gb300 import binding as B
+from online_kv_cache_chunked_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csmkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names == sorted([
+        "csm_workspace_bytes", "csm_compress", "csm_compress_ex", "csm_max_chunks", "csm_append_workspace_bytes",
+        "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "csm_budget", "csm_should_trigger",
+        "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
+        "csmkv_clear_status", "csmkv_status_str"]), names
+    raw = ctypes.CDLL(_build.OUT)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in csmkv.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert B.status_str(code) not in ("", "unknown status")
+    assert B.status_str(99) == "unknown status"
+
+
+@pytest.mark.parametrize("r,c", [(0.5, 256), (0.45, 256), (0.4, 256), (0.1, 256), (0.25, 8), (0.5, 64),
+                                 (0.3, 10), (0.0, 256), (0.2, 256), (0.19999999999999996, 256)])
+def test_edges_per_chunk_matches_oracle(lib, r, c):
+    assert B.csm_edges_per_chunk(r, c) == oracle.edges_per_chunk(r, c)
+
+
+def test_host_helpers_match_oracle(lib):
+    for n, R, G in [(16384, 0.2, 1000), (32768, 0.2, 1000), (65536, 0.2, 1000), (8192, 0.25, 512)]:
+        assert math.isclose(B.csm_budget(n, R, G), oracle.budget(n, R, G), rel_tol=0, abs_tol=1e-9)
+    for j in range(12):
+        assert B.csm_ratio(j, 0.5, 0.05, 0.1) == oracle.ratio(j, 0.5, 0.05, 0.1)
+    for s in [0, 10, 79, 80, 335, 336, 16384, 32897, 65536]:
+        for m in (0, 51, 128):
+            assert B.csm_len_after(s, 16, 64, 256, m) == oracle.len_after(s, 16, 64, 256, m)
+        assert B.csm_num_chunks(s, 16, 64, 256) == osched.num_chunks(s, 16, 64, 256)
+    for s in (3540, 3541):
+        assert B.csm_should_trigger(s, 3476.8, 64) == oracle.should_trigger(s, 3476.8, 64)
+
+
+@pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
+def test_pipeline_plan_matches_oracle_schedule(lib, name):
+    from online_kv_cache_chunked_gb300.pipeline import plan
+    w = synth.WORKLOADS[name]
+    got = plan(w)
+    if w.forced_round:
+        assert [(r.step, r.m) for r in got] == [(0, B.csm_edges_per_chunk(w.r_init, w.c))]
+        return
+    for i, n in enumerate(w.n):
+        ref = osched.plan(n, w.R, w.steps, w.g, w.n1, w.n2, w.c, w.r_init, w.dr, w.r_min)
+        mine = [(r.step, r.s_before[r.seqs.index(i)], r.m, r.s_after[r.seqs.index(i)]) for r in got if i in r.seqs]
+        assert mine == [(st, s, m, s2) for st, s, _, m, s2 in ref]
+
+
+def _cache(**kw):
+    d = dict(batch=1, h_kv=2, head_dim=128, cap=1024, dtype=0)
+    d.update(kw)
+    return B.Cache(d["batch"], d["h_kv"], d["head_dim"], d["cap"], d["dtype"])
+
+
+def _compress(lib, cache, n1=16, n2=64, c=256, r=0.5, ptr=4096, ws=1 << 20, wsp=1 << 16):
+    P = ctypes.c_void_p
+    return lib.csm_compress(P(ptr), P(ptr), P(ptr), P(ptr), ctypes.byref(cache), n1, n2, c, r, None, None,
+                            P(wsp), ws, None)
+
+
+def test_csm_argument_errors_without_gpu(lib):
+    c = _cache()
+    assert _compress(lib, c, r=0.6) == 1
+    assert _compress(lib, c, r=-0.1) == 1
+    assert _compress(lib, c, r=float("nan")) == 1
+    assert _compress(lib, c, c=7) == 1
+    assert _compress(lib, c, c=512) == 1
+    assert _compress(lib, c, n1=-1) == 1
+    assert _compress(lib, _cache(cap=1020)) == 1          # cap % 8
+    assert _compress(lib, _cache(head_dim=100)) == 1      # head_dim % 8
+    assert _compress(lib, _cache(head_dim=256)) == 1      # head_dim > 128
+    assert _compress(lib, _cache(dtype=5)) == 2
+    assert _compress(lib, c, ptr=4100) == 3               # misaligned
+    assert _compress(lib, c, ws=16) == 5                  # workspace too small
+    assert _compress(lib, c, wsp=4096 + 16) == 5          # workspace misaligned
+    need = lib.csm_workspace_bytes(ctypes.byref(c), 16, 64, 256)
+    assert need > 256
+    assert lib.csm_max_chunks(ctypes.byref(c), 16, 64, 256) == (1024 - 80) // 256
+
+
+def test_attention_argument_errors_without_gpu(lib):
+    P = ctypes.c_void_p
+    c = _cache()
+
+    def call(h_q=8, scale=0.088, ptr=4096, cache=c):
+        return lib.decode_attn_logn(P(ptr), P(ptr), P(ptr), P(ptr), P(ptr), ctypes.byref(cache), h_q, scale,
+                                    P(ptr), P(1 << 16), 1 << 24, None)
+    assert call(h_q=3) == 1          # not a multiple of h_kv
+    assert call(h_q=0) == 1
+    assert call(scale=0.0) == 1
+    assert call(ptr=4104) == 3
+    assert call(h_q=18) == 8         # bf16 group of 9 query heads is not covered
+    assert call(cache=_cache(head_dim=96)) == 8
+    assert lib.csm_append(None, None, None, None, ctypes.byref(c), None, None, None, None, 0, None) == 1

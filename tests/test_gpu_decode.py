@@ -1,0 +1,134 @@
+"""Degree-aware decode attention and append on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_kv_cache_chunked_gb300 import binding as B
+from online_kv_cache_chunked_gb300 import synth
+from tests.gpu_helpers import attn_parity, round_parity, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def _attn(q, K, V, N, L):
+    cache = B.cache_desc(K)
+    ws = B.new_workspace(B.decode_attn_workspace_bytes(cache, q.shape[1]))
+    out = torch.full((q.shape[0], q.shape[1], K.shape[3]), float("nan"), dtype=K.dtype, device=K.device)
+    B.decode_attn_logn(q, K, V, N, L, out, ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0
+    return out
+
+
+def _case(rng, batch, h_kv, G, cap, D, lengths, dtype=torch.bfloat16, degrees=True, garbage=True):
+    K = torch.randn(batch, h_kv, cap, D, device="cuda").to(dtype)
+    V = torch.randn(batch, h_kv, cap, D, device="cuda").to(dtype)
+    N = torch.from_numpy(rng.integers(1, 50, (batch, h_kv, cap)).astype(np.int32)).cuda() if degrees else \
+        torch.ones(batch, h_kv, cap, dtype=torch.int32, device="cuda")
+    L = torch.tensor(lengths, dtype=torch.int32, device="cuda").view(batch, h_kv)
+    if garbage:  # rows past len hold anything, NaN included
+        for b in range(batch):
+            for h in range(h_kv):
+                s = int(L[b, h])
+                K[b, h, s:] = float("nan")
+                V[b, h, s:] = float("nan")
+    q = (torch.randn(batch, h_kv * G, D, device="cuda") * 1.5).to(dtype)
+    return q, K, V, N, L
+
+
+@pytest.mark.parametrize("G,D", [(4, 128), (7, 128), (1, 128), (8, 128), (4, 64), (2, 64)])
+def test_ragged_lengths_and_degrees(cuda_lib, G, D):
+    rng = np.random.default_rng(G * 100 + D)
+    lengths = [[0, 1, 63, 64, 65, 1000, 4099, 777], [16, 3000, 2, 129, 5000, 0, 64 * 9, 1]]
+    q, K, V, N, L = _case(rng, 2, 8, G, 5120, D, lengths)
+    out = _attn(q, K, V, N, L)
+    attn_parity(q, K, V, N, L, out, "bf16")
+
+
+def test_unit_degrees_long_context(cuda_lib):
+    rng = np.random.default_rng(1)
+    q, K, V, N, L = _case(rng, 1, 8, 4, 33000, 128, [[32768, 32000, 100, 31111, 5, 32999, 16384, 1]],
+                          degrees=False, garbage=False)
+    out = _attn(q, K, V, N, L)
+    attn_parity(q, K, V, N, L, out, "bf16")
+
+
+def test_fp32_path(cuda_lib):
+    rng = np.random.default_rng(2)
+    q, K, V, N, L = _case(rng, 2, 3, 3, 600, 64, [[545, 0, 17], [600, 1, 333]], dtype=torch.float32)
+    out = _attn(q, K, V, N, L)
+    attn_parity(q, K, V, N, L, out, "f32")
+
+
+def test_unsupported_group_size(cuda_lib):
+    rng = np.random.default_rng(3)
+    q, K, V, N, L = _case(rng, 1, 2, 9, 64, 128, [[10, 10]])
+    with pytest.raises(B.CsmkvError) as e:
+        _attn(q, K, V, N, L)
+    assert e.value.code == 8
+
+
+def test_duplicate_clusters_equal_full_attention_on_gpu(cuda_lib):
+    # CSM on a cache whose A tokens duplicate their partners, then log-N attention
+    # over the compressed cache must equal softmax attention over the original
+    rng = np.random.default_rng(4)
+    n1, n2, c, D, G = 16, 64, 256, 128, 4
+    s = n1 + 6 * c + 40 + n2
+    K = torch.randn(1, 2, 2048, D, device="cuda").to(torch.bfloat16)
+    V = torch.randn(1, 2, 2048, D, device="cuda").to(torch.bfloat16)
+    for j in range(6):
+        base = n1 + j * c
+        K[:, :, base:base + c:2] = K[:, :, base + 1:base + c:2]
+        V[:, :, base:base + c:2] = V[:, :, base + 1:base + c:2]
+    N = torch.ones(1, 2, 2048, dtype=torch.int32, device="cuda")
+    L = torch.full((1, 2), s, dtype=torch.int32, device="cuda")
+    q = torch.randn(1, 2 * G, D, device="cuda").to(torch.bfloat16)
+    full = _attn(q, K, V, N, L)
+    round_parity(K, V, N, L, n1, n2, c, 0.5, "bf16", max_dev_frac=1.0)
+    assert int(L[0, 0]) == s - 6 * 128
+    comp = _attn(q, K, V, N, L)
+    assert float((comp.float() - full.float()).abs().max()) <= 2e-2
+
+
+def test_append_and_capacity(cuda_lib):
+    K = torch.zeros(2, 3, 16, 64, dtype=torch.bfloat16, device="cuda")
+    V = torch.zeros_like(K)
+    N = torch.zeros(2, 3, 16, dtype=torch.int32, device="cuda")
+    L = torch.tensor([[0, 5, 15], [16, 3, 8]], dtype=torch.int32, device="cuda")
+    kn = torch.randn(2, 3, 64, device="cuda").to(torch.bfloat16)
+    vn = torch.randn(2, 3, 64, device="cuda").to(torch.bfloat16)
+    ws = B.new_workspace(B.csm_append_workspace_bytes())
+    pre = [to64(K).reshape(6, 16, 64), to64(V).reshape(6, 16, 64), N.cpu().numpy().reshape(6, 16),
+           L.cpu().numpy().reshape(6)]
+    B.csm_append(K, V, N, L, kn, vn, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 4  # the full unit reports CSMKV_ERR_CAPACITY
+    k2, v2, n2, l2, full = oracle.append(*pre, to64(kn).reshape(6, 64), to64(vn).reshape(6, 64))
+    assert full == 1
+    assert np.array_equal(L.cpu().numpy().reshape(6), l2)
+    assert np.array_equal(to64(K).reshape(6, 16, 64), k2) and np.array_equal(to64(V).reshape(6, 16, 64), v2)
+    assert np.array_equal(N.cpu().numpy().reshape(6, 16), n2)
+    # seq_mask appends only the selected sequences
+    B.csmkv_clear_status(ws)
+    B.csm_append(K, V, N, L, kn, vn, seq_mask=torch.tensor([1, 0], dtype=torch.uint8, device="cuda"), workspace=ws)
+    torch.cuda.synchronize()
+    assert L.cpu().tolist() == [[2, 7, 16], [16, 4, 9]]
+    assert B.csmkv_device_status(ws) == 0
+
+
+def test_full_64k_stack_decode_sampled(cuda_lib):
+    """Full-size attention after the prefill rounds, sampled units checked by the oracle."""
+    w = synth.WORKLOADS["llama_64k_32l"]
+    d = synth.make_device(w)
+    from online_kv_cache_chunked_gb300.pipeline import Pipeline
+    p = Pipeline(w, d)
+    p.run(steps=3)
+    torch.cuda.synchronize()
+    assert d["len"].cpu().unique().tolist() == [8323]
+    out = p.out[2]
+    rng = np.random.default_rng(0)
+    layers = sorted(set(int(x) for x in rng.integers(0, w.batch, 4)))
+    for b in layers:
+        sl = slice(b, b + 1)
+        attn_parity(d["q"][2][sl], d["K"][sl], d["V"][sl], d["N"][sl], d["len"][sl], out[sl], "bf16")
