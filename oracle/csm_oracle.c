@@ -306,7 +306,13 @@ int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
     const size_t rec = (size_t)maxch * (c / 2);
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
     for (int32_t u = 0; u < BH; ++u) {
-        if (skip && skip[u]) continue;
+        if (skip && skip[u]) { /* untouched: every row stays where it is */
+            for (int32_t t = 0; t < len[u]; ++t) {
+                if (origin) origin[(size_t)u * cap + t] = t;
+                if (merged) merged[(size_t)u * cap + t] = 0;
+            }
+            continue;
+        }
         int rc = csm_unit(K + (size_t)u * cap * d, V + (size_t)u * cap * d,
                           N + (size_t)u * cap, len + u, cap, d, n1, n2, c, m,
                           forced ? forced + u * rec : NULL,

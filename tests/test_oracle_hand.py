@@ -67,3 +67,16 @@ def test_forced_replay_applies_given_decisions():
     assert out["N"][0, :6].tolist() == [2, 1, 1, 1, 1, 2]
     with pytest.raises(ValueError):  # wrong edge count is rejected
         oracle.csm_round(K, V, N, [8], 0, 0, 8, 2, forced=np.array([[[0, 1, 2, -1]]], np.int32))
+
+
+def test_origin_and_merged_records():
+    case = CASES[0]  # K1_r025: rows 0 and 2 merge into rows 1 and 3
+    K = arr(case["K"])[None]
+    V = np.zeros_like(K)
+    N = np.ones((1, 8), np.int32)
+    out = oracle.csm_round(K, V, N, [8], 0, 0, 8, 2)
+    assert out["origin"][0, :6].tolist() == [1, 3, 4, 5, 6, 7]
+    assert out["merged"][0, :6].tolist() == [1, 1, 0, 0, 0, 0]
+    skipped = oracle.csm_round(K, V, N, [8], 0, 0, 8, 2, skip=[1])
+    assert skipped["origin"][0, :8].tolist() == list(range(8))
+    assert skipped["merged"][0, :8].tolist() == [0] * 8
