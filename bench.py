@@ -1,0 +1,483 @@
+"""Benchmark: CSM compression throughput and degree-aware decode-attention HBM bandwidth.
+
+One step is one pass of the whole hot path over the workload (default: 32
+independent Llama-3.1-8B-shaped layers, 8 KV / 32 q heads, d=128, bf16, 64K
+prefill, 1000 decode steps):
+  restore the prefill cache (device copy from a pristine replica),
+  the CSM rounds the trigger fires after prefill,
+  1000 x [append the step's k, v; log-N decode attention; triggered CSM rounds].
+CSM and attention calls are bracketed by CUDA events on the launching stream.
+
+value         = CSM KV tokens compressed per second of CSM device time (a token is
+                one row of one layer's cache of one sequence, all its KV heads);
+decode_attn   = algorithmic bytes of the attention calls / their device time;
+roofline      = the attention call (the dominant kernel) against measured HBM peak;
+e2e           = the same CSM metric through the C ABI from pinned host buffers
+                (H2D of the prefill cache, the prefill round, D2H of the compacted
+                cache), plus attention decode steps from host buffers;
+cpu_baseline  = the fp64 oracle on the host cores on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSM KV tokens compressed/s; log-N decode-attn HBM GB/s (% of peak), 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def row_bytes(w):
+    e = 2 if w.dtype == "bf16" else 4
+    return 2 * w.d * e + 4
+
+
+def csm_call_stats(w, rd, head_mask):
+    """Tokens and algorithmic bytes of one CSM call (per the round's sequences)."""
+    rb = row_bytes(w)
+    active_heads = w.h_kv - int(np.asarray(head_mask).sum())
+    tokens = 0
+    nbytes = 0
+    for s in rd.s_before:
+        mid = max(0, s - w.n1 - w.n2)
+        ch = mid // w.c
+        tail = s - (w.n1 + ch * w.c) if ch else 0
+        tokens += s * w.layers
+        per_head = ch * w.c * rb + ch * (w.c - rd.m) * rb + 2 * tail * rb
+        nbytes += per_head * active_heads * w.layers
+    return tokens, nbytes
+
+
+def attn_bytes(w, lengths_units):
+    e = 2 if w.dtype == "bf16" else 4
+    return int(lengths_units.sum()) * row_bytes(w) + w.batch * w.h_q * w.d * e * 2
+
+
+def source_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_record(kernel_file):
+    """ncu DRAM bytes per launch for a kernel, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(os.path.basename(kernel_file))
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "online_kv_cache_chunked_gb300", "csrc", os.path.basename(kernel_file))
+    return rec.get("bytes_per_launch") if rec.get("source_sha") == source_sha(src) else None
+
+
+class Clocks:
+    """Samples nvidia-smi during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, units=16, threads=None):
+    """The fp64 oracle's prefill CSM round on a bounded sample of the workload's units
+    (the first 2 layers' 16 KV heads, generated with the same recipe); tokens/s."""
+    import oracle
+    from online_kv_cache_chunked_gb300 import synth
+
+    layers = max(1, units // w.h_kv)
+    ws = synth.scaled(w, layers=layers, seqs=1, n=(w.n[0],), steps=1, name=w.name + "_sample")
+    data = synth.make_numpy(ws)
+    BH = ws.batch * ws.h_kv
+    n = ws.n[0]
+    cap = ws.cap
+    K = np.zeros((BH, cap, ws.d))
+    V = np.zeros((BH, cap, ws.d))
+    K[:, :n] = data["K"].reshape(BH, -1, ws.d)[:, :n]
+    V[:, :n] = data["V"].reshape(BH, -1, ws.d)[:, :n]
+    if ws.dtype == "bf16":  # the oracle sees exactly the stored bf16 values
+        import torch
+        K = torch.from_numpy(K).to(torch.bfloat16).to(torch.float64).numpy()
+        V = torch.from_numpy(V).to(torch.bfloat16).to(torch.float64).numpy()
+    N = np.ones((BH, cap), np.int32)
+    L = np.full(BH, n, np.int32)
+    m = oracle.edges_per_chunk(w.r_init, w.c)
+    nth = oracle.max_threads() if threads is None else threads
+    t0 = time.perf_counter()
+    oracle.csm_round(K, V, N, L, ws.n1, ws.n2, ws.c, m, nthreads=nth)
+    dt = time.perf_counter() - t0
+    tokens = n * layers  # tokens per (layer, sequence) cache, all KV heads
+    return dict(value=tokens / dt, unit="tokens/s", cores=nth, seconds=dt,
+                sample=f"prefill CSM round (s={n}, c={w.c}, m={m}) of {BH} (layer, KV head) units "
+                       f"= {layers} layers x {w.h_kv} heads of the {w.layers}-layer stack, fp64 oracle")
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def aggregate(local, world, dist_mod=None):
+    """Whole-job numbers: units summed over ranks, times max over ranks."""
+    if world == 1:
+        return dict(local)
+    import torch
+
+    keys_sum = ["tokens", "attn_bytes", "steps_done"]
+    keys_max = ["elapsed_s", "csm_s", "attn_s"]
+    v_sum = torch.tensor([float(local[k]) for k in keys_sum], dtype=torch.float64)
+    v_max = torch.tensor([float(local[k]) for k in keys_max], dtype=torch.float64)
+    dm = dist_mod
+    if dm is None:
+        import torch.distributed as dm
+    dev = "cuda" if dm.get_backend() == "nccl" else "cpu"
+    v_sum, v_max = v_sum.to(dev), v_max.to(dev)
+    dm.all_reduce(v_sum, op=dm.ReduceOp.SUM)
+    dm.all_reduce(v_max, op=dm.ReduceOp.MAX)
+    out = dict(local)
+    out.update({k: float(x) for k, x in zip(keys_sum, v_sum.cpu().tolist())})
+    out.update({k: float(x) for k, x in zip(keys_max, v_max.cpu().tolist())})
+    return out
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores (the reference arm)."""
+    from online_kv_cache_chunked_gb300 import synth
+
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(w, units=args.ref_units)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = oracle_sample(w, units=args.ref_units)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+    tokens_per_step = r["value"] * r["seconds"]
+    value = tokens_per_step * len(secs) / sum(secs)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * sum(secs) / len(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "layers": w.layers, "sequences": w.seqs, "kv_heads": w.h_kv, "q_heads": w.h_q,
+            "head_dim": w.d, "prefill_tokens": list(w.n) if len(set(w.n)) > 1 else w.n[0],
+            "decode_steps": w.steps, "cache_dtype": w.dtype, "n1": w.n1, "n2": w.n2, "c": w.c, "R": w.R,
+            "r_init": w.r_init, "delta_r": w.dr, "r_min": w.r_min, "g": w.g, "outlier_frac": w.outlier_frac,
+            "parallelism": "independent replicas per GPU (no collective)",
+            "l2": "inputs larger than L2: each decode step reads ~1.1 GB of cache, each prefill round ~13 GB"}
+
+
+def run_gpu(args):
+    import torch
+
+    from online_kv_cache_chunked_gb300 import _build
+    from online_kv_cache_chunked_gb300 import binding as B
+    from online_kv_cache_chunked_gb300 import synth
+    from online_kv_cache_chunked_gb300.pipeline import Pipeline
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    if not os.path.exists(_build.OUT):
+        _build.build()
+    B.load()
+    w = synth.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    d = synth.make_device(w)
+    K0, V0, N0, L0 = (d[k].clone() for k in ("K", "V", "N", "len"))
+    p = Pipeline(w, d, stream=None)
+    head_mask = d["head_mask"].cpu().numpy()
+    rounds = p.rounds
+
+    # host mirror of every unit's length at each attention call
+    from online_kv_cache_chunked_gb300.pipeline import plan  # noqa: F401
+    comp = np.array(w.n, np.int64)
+    attn_len = []
+    ri = 0
+    for step in range(0, w.steps + 1):
+        if step > 0:
+            comp += 1
+            lens = np.zeros((w.batch, w.h_kv), np.int64)
+            for b in range(w.batch):
+                i = b % w.seqs
+                lens[b] = np.where(head_mask.astype(bool), w.n[i] + step, comp[i])
+            attn_len.append(lens)
+        while ri < len(rounds) and rounds[ri].step == step:
+            for i, sa in zip(rounds[ri].seqs, rounds[ri].s_after):
+                comp[i] = sa
+            ri += 1
+    attn_bytes_step = sum(attn_bytes(w, x) for x in attn_len)
+    csm_stats = [csm_call_stats(w, rd, head_mask) for rd in rounds]
+    csm_tokens_step = sum(t for t, _ in csm_stats)
+    csm_bytes_step = sum(b_ for _, b_ in csm_stats)
+
+    ev_pool = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (len(rounds) + w.steps) + 8)]
+    marks = []
+
+    def hook(kind, what, before):
+        e = ev_pool[len(marks)]
+        e.record(stream)
+        marks.append((kind, before, e))
+
+    def one_step(timed):
+        for dst, src in ((d["K"], K0), (d["V"], V0), (d["N"], N0), (d["len"], L0)):
+            dst.copy_(src, non_blocking=True)
+        marks.clear()
+        p.run(hook=hook if timed else None)
+
+    for _ in range(args.warmup):
+        one_step(False)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    csm_ms = attn_ms = 0.0
+    attn_calls = 0
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            one_step(True)
+            torch.cuda.synchronize()
+            for k in range(0, len(marks), 2):
+                kind, _, e0 = marks[k]
+                _, _, e1 = marks[k + 1]
+                dt = e0.elapsed_time(e1)
+                if kind == "csm":
+                    csm_ms += dt
+                else:
+                    attn_ms += dt
+                    attn_calls += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    for ws in (p.ws_csm, p.ws_app, p.ws_att):
+        st = B.csmkv_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {B.status_str(st)}")
+    if not np.array_equal(d["len"].cpu().numpy(), attn_len[-1]):
+        raise RuntimeError("device lengths disagree with the host schedule")
+
+    local_res = dict(tokens=csm_tokens_step * args.steps, attn_bytes=attn_bytes_step * args.steps,
+                     steps_done=args.steps, elapsed_s=elapsed_ms / 1e3, csm_s=csm_ms / 1e3, attn_s=attn_ms / 1e3)
+    agg = aggregate(local_res, world)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args) if rank == 0 else None
+    clocks = clk.summary()
+    if rank != 0:
+        return 0
+    hbm, kind = peaks()
+    attn_gbs = agg["attn_bytes"] / agg["attn_s"] / 1e9
+    per_launch_bytes = attn_bytes_step / w.steps
+    avg_launch_s = (attn_ms / 1e3) / max(1, attn_calls)
+    csm_gbs = csm_bytes_step * args.steps / (csm_ms / 1e3) / 1e9
+    cpu = oracle_sample(w, units=args.ref_units) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC,
+        "value": agg["tokens"] / agg["csm_s"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded AR(1) keys, N(0,1) values, N(0,I) queries; no model weights)",
+        "config": config_of(w),
+        "decode_attn": {"value": attn_gbs, "unit": "GB/s", "frac_of_measured_peak": attn_gbs / hbm,
+                        "frac_of_nominal_7900": attn_gbs / 7900.0, "calls_timed": attn_calls,
+                        "avg_call_us": 1e6 * avg_launch_s},
+        "roofline": {"bound": "hbm", "achieved": per_launch_bytes / avg_launch_s / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": per_launch_bytes / avg_launch_s / 1e9 / hbm,
+                     "traffic": traffic_record("decode_attn.cu"), "kernel": "decode_attn_logn",
+                     "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
+        "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
+                         "traffic": traffic_record("csm_compress.cu"), "kernel": "csm_compress",
+                         "peak_kind": kind, "bytes_per_step": csm_bytes_step},
+        "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
+                "ms_per_step": csm_ms / args.steps, "rounds_per_step": len(rounds)},
+        "e2e": e2e,
+        "gpu_launches": args.steps * (2 * len(rounds) + 4 * w.steps),
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": cpu["value"], "unit": "tokens/s", "cores": cpu["cores"], "kind": "oracle",
+                                "sample": cpu["sample"], "seconds": cpu["seconds"]}
+    print(json.dumps(line))
+    return 0
+
+
+def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
+    """CSM end to end from pinned host buffers: H2D of the prefill cache, the prefill
+    round(s), D2H of the compacted rows; and attention decode steps from host buffers."""
+    import torch
+
+    from online_kv_cache_chunked_gb300 import binding as B
+
+    hK = torch.empty_like(K0, device="cpu").pin_memory()
+    hV = torch.empty_like(V0, device="cpu").pin_memory()
+    hN = torch.empty_like(N0, device="cpu").pin_memory()
+    hL = torch.empty_like(L0, device="cpu").pin_memory()
+    hK.copy_(K0)
+    hV.copy_(V0)
+    hN.copy_(N0)
+    hL.copy_(L0)
+    pre = [rd for rd in rounds if rd.step == 0]
+    s_after = pre[-1].s_after[0] if pre else w.n[0]
+    BH = w.batch * w.h_kv
+    oK = torch.empty((BH, s_after, w.d), dtype=K0.dtype).pin_memory()
+    oV = torch.empty((BH, s_after, w.d), dtype=V0.dtype).pin_memory()
+    oN = torch.empty((BH, s_after), dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream()
+    tokens = sum(csm_call_stats(w, rd, d["head_mask"].cpu().numpy())[0] for rd in pre)
+    times = []
+    for it in range(args.warmup + max(1, args.steps)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        d["K"].copy_(hK, non_blocking=True)
+        d["V"].copy_(hV, non_blocking=True)
+        d["N"].copy_(hN, non_blocking=True)
+        d["len"].copy_(hL, non_blocking=True)
+        p.compress_at(0)
+        oK.copy_(d["K"].view(BH, -1, w.d)[:, :s_after], non_blocking=True)
+        oV.copy_(d["V"].view(BH, -1, w.d)[:, :s_after], non_blocking=True)
+        oN.copy_(d["N"].view(BH, -1)[:, :s_after], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
+    d2h = sum(t.numel() * t.element_size() for t in (oK, oV, oN))
+    # attention decode steps from host buffers: H2D of q, k, v; append; attend; D2H of o
+    nsteps = min(50, w.steps)
+    hq = d["q"][:nsteps].cpu().pin_memory()
+    hk = d["k_dec"][:nsteps].cpu().pin_memory()
+    hv = d["v_dec"][:nsteps].cpu().pin_memory()
+    ho = torch.empty_like(p.out[:nsteps], device="cpu").pin_memory()
+    dq, dk, dv = torch.empty_like(d["q"][0]), torch.empty_like(d["k_dec"][0]), torch.empty_like(d["v_dec"][0])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(nsteps):
+        dq.copy_(hq[i], non_blocking=True)
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        B.csm_append(d["K"], d["V"], d["N"], d["len"], dk, dv, None, p.ws_app)
+        B.decode_attn_logn(dq, d["K"], d["V"], d["N"], d["len"], p.out[i], p.ws_att)
+        ho[i].copy_(p.out[i], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    lens = d["len"].cpu().numpy()
+    step_bytes = attn_bytes(w, lens - nsteps // 2)
+    att_s = e0.elapsed_time(e1) / 1e3
+    return {"value": tokens / float(np.median(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
+            "compress, D2H compacted rows",
+            "decode_attn_gbs": step_bytes * nsteps / att_s / 1e9,
+            "decode_step_h2d_bytes": int(dq.numel() * dq.element_size() * 1 + 2 * dk.numel() * dk.element_size()),
+            "decode_step_d2h_bytes": int(ho[0].numel() * ho[0].element_size())}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="llama_64k_32l")
+    ap.add_argument("--ref-units", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -114,7 +114,12 @@ def test_append_and_capacity(cuda_lib):
     B.csm_append(K, V, N, L, kn, vn, seq_mask=torch.tensor([1, 0], dtype=torch.uint8, device="cuda"), workspace=ws)
     torch.cuda.synchronize()
     assert L.cpu().tolist() == [[2, 7, 16], [16, 4, 9]]
-    assert B.csmkv_device_status(ws) == 0
+    assert B.csmkv_device_status(ws) == 4  # unit (0, 2) filled up on the first append
+    B.csmkv_clear_status(ws)
+    L.copy_(torch.tensor([[1, 1, 1], [1, 1, 1]], dtype=torch.int32))
+    B.csm_append(K, V, N, L, kn, vn, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0 and L.cpu().tolist() == [[2, 2, 2], [2, 2, 2]]
 
 
 def test_full_64k_stack_decode_sampled(cuda_lib):
