@@ -13,8 +13,11 @@
 // warps each take 16 tokens of a tile and run S^T = K q^T and O^T += V^T P^T on
 // mma.sync (bf16 in, fp32 accumulate), the G <= 8 query heads of the group in
 // the N = 8 dimension, so each K/V byte is read once for the whole group. Each
-// warp writes one partial (m, l, acc) per unit it touched; a combine kernel
-// merges the partials of a unit into the output.
+// warp writes one partial (m, l, acc) per unit it touched; the last CTA to
+// finish its part of a unit (a per-unit counter) merges the unit's partials into
+// the output. Unit offsets come from a block-wide scan of the lengths inside
+// every CTA (or, for batches of more than 2048 units, from a one-CTA prologue).
+// After a device error the workspace must be zero-filled again before reuse.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -30,6 +33,7 @@ constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
 constexpr int kDecCtasPerSm = 2;
 constexpr int kSlotHeads = 8;  // partial records are padded to 8 heads
+constexpr int kMaxScanUnits = 2048;  // units whose offsets a CTA scans itself
 
 struct DecParams {
     const void* q;
@@ -41,6 +45,7 @@ struct DecParams {
     float* pm;            // [slots][8] running max (base-2 domain)
     float* pl;            // [slots][8] running sum
     float* pacc;          // [slots][8][D] unnormalised output
+    int32_t* counter;     // [BH] parts of a unit finished in this call; the last one resets it
     int32_t BH, Hkv, Hq, G, cap, D, nCTA;
     float scale_log2;     // scale * log2(e)
     float scale;          // natural-log scale (fp32 path)
@@ -140,7 +145,70 @@ struct RangeWalker {
     }
 };
 
+// Scratch of the main kernel after the stage ring.
+struct DecSmall {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int abort_flag;
+    int last;      // this CTA is the last contributor of the unit being closed
+    int u0;        // first unit of the CTA's range
+    int total;
+    int warp_tot[kDecThreads / 32];
+};
+
+__device__ __forceinline__ void consumer_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Merges the partials of `unit` (written by CTAs c0..c1, 4 warps each) into the
+// output; run by the 4 consumer warps of the last contributing CTA.
 template <int D>
+__device__ void combine_unit(const DecParams& p, int unit, int c0, int c1, int warp, int lane) {
+    constexpr int PER = D / 32;  // output dims per lane
+    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
+    for (int g = warp; g < p.G; g += kConsumerWarps) {
+        float M = -INFINITY;
+        for (int c = c0; c <= c1; ++c)
+            for (int w = 0; w < kConsumerWarps; ++w)
+                M = fmaxf(M, __ldcg(p.pm + (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + g));
+        float acc[PER], L = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+        for (int c = c0; c <= c1; ++c)
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const size_t rec = (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + g;
+                const float mw = __ldcg(p.pm + rec);
+                if (mw == -INFINITY) continue;  // that warp saw no token of the unit
+                const float f = exp2f(mw - M);
+                L = fmaf(f, __ldcg(p.pl + rec), L);
+                const float* a = p.pacc + rec * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(a));
+                    acc[0] = fmaf(f, v.x, acc[0]);
+                    acc[1] = fmaf(f, v.y, acc[1]);
+                    acc[2] = fmaf(f, v.z, acc[2]);
+                    acc[3] = fmaf(f, v.w, acc[3]);
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(a));
+                    acc[0] = fmaf(f, v.x, acc[0]);
+                    acc[1] = fmaf(f, v.y, acc[1]);
+                }
+            }
+        const float inv = 1.0f / L;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D +
+                           lane * PER;
+        if constexpr (PER == 4) {
+            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                      pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        } else {
+            *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+    }
+}
+
+// SCAN: the CTA computes the unit offsets itself (units <= kMaxScanUnits, kept in
+// shared memory); otherwise decode_prologue_kernel has written them to the workspace.
+template <int D, bool SCAN>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     decode_main_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN) {
@@ -148,17 +216,92 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* const sbase =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* const full = reinterpret_cast<uint64_t*>(sbase + kStages * Geo::kStageBytes);
-    uint64_t* const empty = full + kStages;
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    DecSmall& sm = *reinterpret_cast<DecSmall*>(sbase + kStages * Geo::kStageBytes);
+    int* const sPrefix = reinterpret_cast<int*>(&sm + 1);
+    uint64_t* const full = sm.full;
+    uint64_t* const empty = sm.empty;
+    volatile int* const abort_flag = &sm.abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int W = p.hdr->tokens_per_cta;
-    const int total = p.hdr->total_tokens;
+
+    // ---------------------------------------------------------------- unit offsets
+    const int* pre;
+    int total, W;
+    if constexpr (SCAN) {
+        const int per = (p.BH + kDecThreads - 1) / kDecThreads;
+        const int ub = tid * per;
+        int local = 0;
+        for (int i = 0; i < per; ++i) {
+            const int u = ub + i;
+            if (u < p.BH) {
+                int v = p.len[u];
+                if (v < 0 || v > p.cap) {
+                    record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                    v = 0;
+                }
+                local += v;
+            }
+        }
+        int incl = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        if (lane == 31) sm.warp_tot[warp] = incl;
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int w = 0; w < kDecThreads / 32; ++w) {
+                const int t = sm.warp_tot[w];
+                sm.warp_tot[w] = run;
+                run += t;
+            }
+            sm.total = run;
+            sPrefix[p.BH] = run;
+        }
+        __syncthreads();
+        int run = sm.warp_tot[warp] + incl - local;
+        for (int i = 0; i < per; ++i) {
+            const int u = ub + i;
+            if (u < p.BH) {
+                sPrefix[u] = run;
+                const int v = p.len[u];
+                run += (v < 0 || v > p.cap) ? 0 : v;
+            }
+        }
+        __syncthreads();
+        pre = sPrefix;
+        total = sm.total;
+        W = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+    } else {
+        pre = p.prefix;
+        total = p.hdr->total_tokens;
+        W = p.hdr->tokens_per_cta;
+    }
+
+    // Empty units get a zero output from the CTA whose range starts at their offset.
+    for (int u = tid; u < p.BH; u += kDecThreads) {
+        if (pre[u + 1] != pre[u]) continue;
+        if (min(pre[u] / W, (int)gridDim.x - 1) != (int)blockIdx.x) continue;
+        const int b = u / p.Hkv, kv = u - b * p.Hkv;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G) * D;
+        for (int i = 0; i < p.G * D / 8; ++i) reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+
     const int r0 = blockIdx.x * W;
     const int r1 = min(total, r0 + W);
     if (r0 >= r1) return;
-    const int u0 = p.cta_unit[blockIdx.x];
+    int u0;
+    if constexpr (SCAN) {
+        if (tid == 0) sm.u0 = p.BH;
+        __syncthreads();
+        for (int u = tid; u < p.BH; u += kDecThreads)
+            if (pre[u] <= r0 && r0 < pre[u + 1]) sm.u0 = u;
+        __syncthreads();
+        u0 = sm.u0;
+    } else {
+        u0 = p.cta_unit[blockIdx.x];
+    }
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -176,14 +319,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
     if (warp == kConsumerWarps) {
         // ============================================================ producer
-        int issued = 0;
         if (lane == 0) {
-            RangeWalker rw{p.prefix, p.BH, u0, r0, r1};
+            int issued = 0;
+            RangeWalker rw{pre, p.BH, u0, r0, r1};
             int unit, t0, n;
             bool ok = true;
             while (ok && rw.next(unit, t0, n)) {
                 const long long row_base = (long long)unit * p.cap;
-                for (int t = 0; t < n && ok; t += kTile) {
+                for (int t = 0; t < n; t += kTile) {
                     const int s = issued % kStages;
                     if (issued >= kStages) {
                         ok = mbar_wait(&empty[s], ((issued / kStages) - 1) & 1, globaltimer() + budget_ns);
@@ -193,9 +336,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                     uint8_t* st = sbase + s * Geo::kStageBytes;
                     mbar_expect_tx(&full[s], Geo::kTxBytes);
 #pragma unroll
-                    for (int b = 0; b < Geo::kBoxes; ++b) {
-                        tma_load_2d(st + Geo::kKOff + b * Geo::kBoxBytes, &tmK, &full[s], b * 64, row);
-                        tma_load_2d(st + Geo::kVOff + b * Geo::kBoxBytes, &tmV, &full[s], b * 64, row);
+                    for (int bx = 0; bx < Geo::kBoxes; ++bx) {
+                        tma_load_2d(st + Geo::kKOff + bx * Geo::kBoxBytes, &tmK, &full[s], bx * 64, row);
+                        tma_load_2d(st + Geo::kVOff + bx * Geo::kBoxBytes, &tmV, &full[s], bx * 64, row);
                     }
                     tma_load_2d(st + Geo::kNOff, &tmN, &full[s], 0, row >> 2);
                     ++issued;
@@ -219,14 +362,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
     uint32_t qf[D / 16][2];
     float oacc[D / 16][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float m0, m1, l0, l1;
 
-    RangeWalker rw{p.prefix, p.BH, u0, r0, r1};
+    RangeWalker rw{pre, p.BH, u0, r0, r1};
     int unit, t0, n;
     int consumed = 0;
     bool ok = true;
-    while (ok && rw.next(unit, t0, n)) {
-        // query fragments of this unit's group: B[k = dim][n = head g]
+    while (rw.next(unit, t0, n)) {
         const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
         const __nv_bfloat16* qrow = qg + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D;
 #pragma unroll
@@ -247,8 +389,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
         for (int t = 0; t < n; t += kTile) {
             const int s = consumed % kStages;
-            ok = mbar_wait(&full[s], (consumed / kStages) & 1, globaltimer() + budget_ns);
-            if (!ok || *abort_flag) { ok = false; break; }
+            if (!mbar_wait(&full[s], (consumed / kStages) & 1, globaltimer() + budget_ns) || *abort_flag) {
+                ok = false;
+                break;
+            }
             const int nv = min(kTile, n - t);  // valid tokens in this tile
             uint8_t* st = sbase + s * Geo::kStageBytes;
             const int noff = (int)((row_base + t0 + t) & 3);
@@ -328,7 +472,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             if (lane == 0) mbar_arrive(&empty[s]);
             ++consumed;
         }
-        if (!ok) break;
+        // ---- every consumer warp reaches the barriers below, aborted or not
+        if (!ok) *abort_flag = 1;
+        consumer_barrier();
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
         // ---- partial of (this CTA, this unit, this warp)
         float lt0 = l0, lt1 = l1;
 #pragma unroll
@@ -349,55 +499,24 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             if (h0 < p.G) { acc0[16 * mb + g] = oacc[mb][0]; acc0[16 * mb + g + 8] = oacc[mb][2]; }
             if (h1 < p.G) { acc1[16 * mb + g] = oacc[mb][1]; acc1[16 * mb + g + 8] = oacc[mb][3]; }
         }
-    }
-    if (!ok) {
-        if (lane == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
-        *abort_flag = 1;
-    }
-}
-
-// ----------------------------------------------------------------------------
-// Combine: one warp per (unit, query head of the group).
-template <typename T>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecParams p) {
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.BH * p.G) return;
-    const int unit = gw / p.G, gh = gw - unit * p.G;
-    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
-    T* out = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G + gh) * p.D;
-    const int beg = p.prefix[unit], end = p.prefix[unit + 1];
-    if (end <= beg) {
-        for (int d = lane; d < p.D; d += 32) out[d] = T(0.f);
-        return;
-    }
-    const int W = p.hdr->tokens_per_cta;
-    const int c0 = beg / W, c1 = (end - 1) / W;
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c)
-        for (int w = 0; w < kConsumerWarps; ++w)
-            M = fmaxf(M, p.pm[(((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + gh]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
-    for (int c = c0; c <= c1; ++c)
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const size_t rec = (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + gh;
-            const float mw = p.pm[rec];
-            if (mw == -INFINITY) continue;
-            const float f = exp2f(mw - M);
-            L = fmaf(f, p.pl[rec], L);
-            const float* a = p.pacc + rec * p.D;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int d = lane + 32 * i;
-                if (d < p.D) acc[i] = fmaf(f, a[d], acc[i]);
-            }
+        // ---- the last CTA to finish its part of the unit merges every part
+        __threadfence();
+        consumer_barrier();
+        const int c0 = pre[unit] / W, c1 = (pre[unit + 1] - 1) / W;
+        if (tid == 0) {
+            const int prev = atomicAdd(p.counter + unit, 1);
+            const int last = prev == c1 - c0;
+            if (last) p.counter[unit] = 0;  // ready for the next call
+            sm.last = last;
         }
-    const float inv = 1.0f / L;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int d = lane + 32 * i;
-        if (d < p.D) out[d] = T(acc[i] * inv);
+        consumer_barrier();
+        if (sm.last) {
+            __threadfence();
+            combine_unit<D>(p, unit, c0, c1, warp, lane);
+        }
+        consumer_barrier();  // sm.last is rewritten for the next unit
     }
+    if (!ok && tid == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
 }
 
 // ----------------------------------------------------------------------------
@@ -465,8 +584,8 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const DecParams p, cons
     }
 }
 
-static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, size_t* o_cta, size_t* o_pm,
-                         size_t* o_pl, size_t* o_pacc) {
+static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, size_t* o_cta, size_t* o_cnt,
+                         size_t* o_pm, size_t* o_pl, size_t* o_pacc) {
     const size_t BH = (size_t)cache->batch * cache->h_kv;
     const size_t slots = ((size_t)nCTA + BH) * kConsumerWarps;
     size_t off = kHeaderBytes;
@@ -474,6 +593,8 @@ static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, s
     off = align_up(off + (BH + 1) * 4, 256);
     *o_cta = off;
     off = align_up(off + (size_t)nCTA * 4, 256);
+    *o_cnt = off;
+    off = align_up(off + BH * 4, 256);
     *o_pm = off;
     off = align_up(off + slots * kSlotHeads * 4, 256);
     *o_pl = off;
@@ -483,11 +604,12 @@ static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, s
     return off;
 }
 
-template <int D>
+template <int D, bool SCAN>
 static int launch_decode_bf16(const DecParams& P, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tn, cudaStream_t st) {
-    constexpr int smem = kStages * DecGeom<D>::kStageBytes + 2 * kStages * 8 + 16 + 1024;
-    auto kern = decode_main_kernel<D>;
+    constexpr int smem = kStages * DecGeom<D>::kStageBytes + (int)sizeof(DecSmall) +
+                         (SCAN ? (kMaxScanUnits + 1) * 4 : 0) + 1024;
+    auto kern = decode_main_kernel<D, SCAN>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return CSMKV_ERR_CUDA;
     kern<<<P.nCTA, kDecThreads, smem, st>>>(P, tk, tv, tn);
@@ -502,8 +624,8 @@ extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t 
     if (check_cache(cache) != CSMKV_OK || h_q < 1) return 0;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return 0;
-    size_t a, b, c, d, e;
-    return dec_layout(cache, nCTA, &a, &b, &c, &d, &e);
+    size_t a, b, c, d, e, f;
+    return dec_layout(cache, nCTA, &a, &b, &c, &d, &e, &f);
 }
 
 extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
@@ -523,8 +645,8 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
     if (bf16 && (G > 8 || (D != 64 && D != 128))) return CSMKV_ERR_UNSUPPORTED;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return CSMKV_ERR_CUDA;
-    size_t o_prefix, o_cta, o_pm, o_pl, o_pacc;
-    const size_t need = dec_layout(cache, nCTA, &o_prefix, &o_cta, &o_pm, &o_pl, &o_pacc);
+    size_t o_prefix, o_cta, o_cnt, o_pm, o_pl, o_pacc;
+    const size_t need = dec_layout(cache, nCTA, &o_prefix, &o_cta, &o_cnt, &o_pm, &o_pl, &o_pacc);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -538,6 +660,7 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
     P.pm = reinterpret_cast<float*>(ws + o_pm);
     P.pl = reinterpret_cast<float*>(ws + o_pl);
     P.pacc = reinterpret_cast<float*>(ws + o_pacc);
+    P.counter = reinterpret_cast<int32_t*>(ws + o_cnt);
     P.BH = cache->batch * cache->h_kv;
     P.Hkv = cache->h_kv;
     P.Hq = h_q;
@@ -573,10 +696,9 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
                           CU_TENSOR_MAP_SWIZZLE_NONE))
             return CSMKV_ERR_CUDA;
     }
+    if (P.BH <= kMaxScanUnits)
+        return D == 128 ? launch_decode_bf16<128, true>(P, tk, tv, tn, st) : launch_decode_bf16<64, true>(P, tk, tv, tn, st);
     decode_prologue_kernel<<<1, 1024, 0, st>>>(P);
     if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
-    rc = D == 128 ? launch_decode_bf16<128>(P, tk, tv, tn, st) : launch_decode_bf16<64>(P, tk, tv, tn, st);
-    if (rc != CSMKV_OK) return rc;
-    decode_combine_kernel<__nv_bfloat16><<<(P.BH * G + 7) / 8, 256, 0, st>>>(P);
-    return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
+    return D == 128 ? launch_decode_bf16<128, false>(P, tk, tv, tn, st) : launch_decode_bf16<64, false>(P, tk, tv, tn, st);
 }

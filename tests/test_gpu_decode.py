@@ -137,3 +137,30 @@ def test_full_64k_stack_decode_sampled(cuda_lib):
     for b in layers:
         sl = slice(b, b + 1)
         attn_parity(d["q"][2][sl], d["K"][sl], d["V"][sl], d["N"][sl], d["len"][sl], out[sl], "bf16")
+
+
+def test_many_units_use_the_prologue_path(cuda_lib):
+    # more than 2048 (sequence, KV head) units: offsets come from the one-CTA prologue
+    rng = np.random.default_rng(6)
+    lengths = rng.integers(0, 300, (260, 8)).tolist()
+    q, K, V, N, L = _case(rng, 260, 8, 4, 320, 128, lengths, garbage=False)
+    out = _attn(q, K, V, N, L)
+    attn_parity(q, K, V, N, L, out, "bf16")
+
+
+def test_repeated_calls_on_one_workspace(cuda_lib):
+    # the per-unit completion counters reset themselves: calls 2..4 equal call 1
+    rng = np.random.default_rng(8)
+    q, K, V, N, L = _case(rng, 2, 8, 4, 9000, 128, rng.integers(0, 9000, (2, 8)).tolist())
+    cache = B.cache_desc(K)
+    ws = B.new_workspace(B.decode_attn_workspace_bytes(cache, q.shape[1]))
+    outs = []
+    for _ in range(4):
+        o = torch.empty((2, 32, 128), dtype=torch.bfloat16, device="cuda")
+        B.decode_attn_logn(q, K, V, N, L, o, ws)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    attn_parity(q, K, V, N, L, outs[0], "bf16")
