@@ -384,7 +384,7 @@ def run_gpu(args):
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
                 "ms_per_step": csm_ms / args.steps, "rounds_per_step": len(rounds)},
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 * len(rounds) + 4 * w.steps),
+        "gpu_launches": args.steps * (2 * len(rounds) + (2 if w.batch * w.h_kv <= 2048 else 3) * w.steps),
         "clocks": clocks,
     }
     if cpu is not None:
@@ -459,7 +459,7 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     return {"value": tokens / float(np.median(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
             "compress, D2H compacted rows",
-            "decode_attn_gbs": step_bytes * nsteps / att_s / 1e9,
+            "decode_attn_gbs_at_prefill_round_length": step_bytes * nsteps / att_s / 1e9,
             "decode_step_h2d_bytes": int(dq.numel() * dq.element_size() * 1 + 2 * dk.numel() * dk.element_size()),
             "decode_step_d2h_bytes": int(ho[0].numel() * ho[0].element_size())}
 
