@@ -71,12 +71,13 @@ struct Elem<float> {
 // Shared-memory tables of one chunk's decisions.
 struct CsmTables {
     float inv[256];       // inverse key norm per chunk row
-    float best[256];      // per-group best similarity, then final per A row
-    int32_t bestb[256];   // per-group argmax, then final per A row
+    float best[512];      // per-group best similarity, then final per A row
+    int32_t bestb[512];   // per-group argmax, then final per A row
     int32_t match[128];   // B index for selected A rows, else -1
     int32_t cnt[128];     // incoming edges per B row
     int32_t off[128];     // CSR offsets per B row
     int32_t nsum[128];    // merged degree per B row
+    float ninv[128];      // 1 / nsum
     int32_t pre[132];     // selected A rows before index a (pre[H] = m)
     int16_t src[256];     // output row -> chunk row
     uint8_t list[128];    // CSR member list (A indices)
@@ -111,9 +112,13 @@ __device__ __forceinline__ void publish(int32_t* flag, int32_t epoch, int withho
 // From per-group (best, argmax) records to the chunk's merge plan: exactly m
 // selected A rows (similarity desc, A index asc), the output row -> chunk row
 // map, and the CSR list of A rows merging into every B row. All threads call.
+// With H = 128 and 256 or 512 threads, R = blockDim / 128 consecutive threads
+// share one A row's rank count and list position.
 __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int m, int ngroups) {
     const int H = c / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = (H == 128 && blockDim.x >= 256) ? (int)blockDim.x / 128 : 1;  // 1, 2 or 4
+    const int ra = tid / R, rp = tid - ra * R, span = H / R;
     if (tid < H) {  // combine groups in column order: a later group wins only if strictly better
         float best = sm.best[tid];
         int bb = sm.bestb[tid];
@@ -126,19 +131,25 @@ __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int
         sm.cnt[tid] = 0;
     }
     __syncthreads();
-    bool sel = false;
-    if (tid < H) {
-        const float key = sm.best[tid];
+    if (ra < H) {  // rank of A row ra among all A rows, counted over R parts
+        const float key = sm.best[ra];
         int rank = 0;
+        const int a0 = rp * span;
 #pragma unroll 8
-        for (int a2 = 0; a2 < H; ++a2) {
+        for (int i = 0; i < span; ++i) {
+            const int a2 = a0 + i;
             const float k2 = sm.best[a2];
-            rank += (k2 > key) || (k2 == key && a2 < tid);
+            rank += (k2 > key) || (k2 == key && a2 < ra);
         }
-        sel = rank < m;
-        sm.match[tid] = sel ? sm.bestb[tid] : -1;
-        if (sel) atomicAdd(&sm.cnt[sm.bestb[tid]], 1);
+        for (int o = 1; o < R; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (rp == 0) {
+            const bool sel = rank < m;
+            sm.match[ra] = sel ? sm.bestb[ra] : -1;
+            if (sel) atomicAdd(&sm.cnt[sm.bestb[ra]], 1);
+        }
     }
+    __syncthreads();
+    const bool sel = tid < H && sm.match[tid] >= 0;
     {   // exclusive prefix of the selection over A (H <= 128 -> warps 0..3)
         const unsigned bal = __ballot_sync(0xffffffffu, sel);
         if (lane == 0 && warp < 4) sm.misc[3 + warp] = __popc(bal);
@@ -179,11 +190,15 @@ __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int
             sm.src[q - sm.pre[(q >> 1) + 1]] = (int16_t)q;
         }
     }
-    if (tid < H && sel) {
-        const int b = sm.match[tid];
+    if (ra < H) {  // position of a selected A row in its target's list: earlier A rows with the same target
+        const int b = sm.match[ra];
         int r = 0;
-        for (int a2 = 0; a2 < tid; ++a2) r += (sm.match[a2] == b);
-        sm.list[sm.off[b] + r] = (uint8_t)tid;
+        if (b >= 0) {
+            const int a0 = rp * span, a1 = min(a0 + span, ra);
+            for (int a2 = a0; a2 < a1; ++a2) r += (sm.match[a2] == b);
+        }
+        for (int o = 1; o < R; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (b >= 0 && rp == 0) sm.list[sm.off[b] + r] = (uint8_t)ra;
     }
     __syncthreads();
     if (tid < H) {
@@ -191,12 +206,14 @@ __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int
         const int o0 = sm.off[tid], o1 = o0 + sm.cnt[tid];
         for (int k = o0; k < o1; ++k) ns += sN[2 * (int)sm.list[k]];
         sm.nsum[tid] = ns;
+        sm.ninv[tid] = 1.0f / (float)ns;
     }
     __syncthreads();
 }
 
 // Writes the c - m output rows of one array of a chunk: copies, or degree-
-// weighted means for B rows with incoming edges (fp32, rounded once).
+// weighted means for B rows with incoming edges (fp32 sums scaled by the reciprocal
+// of the degree sum, rounded once to the cache dtype).
 // piece(q, cc) gives the 16-byte piece cc of chunk row q in shared memory.
 template <typename T, typename PieceFn>
 __device__ __forceinline__ void emit_rows(T* dst_rows, int rows_out, int D, const CsmTables& sm,
@@ -224,9 +241,9 @@ __device__ __forceinline__ void emit_rows(T* dst_rows, int rows_out, int D, cons
 #pragma unroll
                 for (int e = 0; e < EPP; ++e) acc[e] = fmaf(na, f[e], acc[e]);
             }
-            const float ns = (float)sm.nsum[b];
+            const float inv = sm.ninv[b];  // one reciprocal per merged row
 #pragma unroll
-            for (int e = 0; e < EPP; ++e) acc[e] = acc[e] / ns;
+            for (int e = 0; e < EPP; ++e) acc[e] *= inv;
             val = E::pack(acc);
         } else {
             val = *reinterpret_cast<const uint4*>(piece(q, cc));

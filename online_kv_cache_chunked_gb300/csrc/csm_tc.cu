@@ -12,7 +12,7 @@
 //
 // Per chunk: fp32 inverse key norms; one thread issues d/16 tcgen05.mma
 // (M = N = 128, fp32 accumulate in 128 TMEM columns) for the 128 x 128 dot
-// products; eight warps read them back with tcgen05.ld, scale by the norms and
+// products; sixteen warps read them back with tcgen05.ld, scale by the norms and
 // take the per-A argmax; then the shared top-m selection, merge and compaction.
 // The "loaded" flag of an item is published as soon as its slot's TMA lands, so
 // items that overwrite its source rows wait as little as possible.
@@ -31,6 +31,8 @@ struct TcRing {
     static constexpr int kSmem = kSlots * kSlotBytes + kSlots * kNStride + (int)sizeof(CsmTables) + 64 + 1024;
 };
 
+constexpr int kTcThreads = 512;  // 16 warps: 4 TMEM lane quarters x 4 column groups
+
 struct TcState {
     uint64_t bar[3];  // one per ring slot
     uint64_t mma_bar;
@@ -39,7 +41,7 @@ struct TcState {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kCsmThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     csm_tc_kernel(const __grid_constant__ CsmParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN) {
     using R = TcRing<D>;
@@ -176,17 +178,19 @@ __global__ void __launch_bounds__(kCsmThreads, 1)
                 if (!kn_done_now) publish(fkn + j, epoch, p.withhold);
             }
 
-            // (2) inverse key norms, one chunk row per thread (c = 256 = block size)
+            // (2) inverse key norms, two threads per chunk row (c = 256 rows, 512 threads)
             {
+                const int q = tid >> 1, h = tid & 1;
                 float ss = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < D / 8; ++cc) {
+                for (int i = 0; i < D / 16; ++i) {
                     float f[8];
-                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(kpiece(tid, cc)), f);
+                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(kpiece(q, h * (D / 16) + i)), f);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
                 }
-                sm.inv[tid] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (h == 0) sm.inv[q] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
             }
             __syncthreads();
 
@@ -209,31 +213,28 @@ __global__ void __launch_bounds__(kCsmThreads, 1)
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
             if (tid == 0) mma_pend = false;
             tc_fence_after();
-            {
-                const int qtr = warp & 3, half = warp >> 2;
+            {   // warp w reads TMEM lanes 32(w%4).. (its A rows) and 32 columns 32(w/4)..
+                const int qtr = warp & 3, grp = warp >> 2;
                 const int a = qtr * 32 + lane;
+                const int col0 = grp * 32;
+                float v[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)col0, v);
                 const float inv_a = sm.inv[2 * a];
                 float best = -INFINITY;
-                int bb = half * 64;
+                int bb = col0;
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    float v[32];
-                    const int col0 = half * 64 + cb * 32;
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)col0, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float cs = v[i] * inv_a * sm.inv[2 * (col0 + i) + 1];
-                        if (cs > best) { best = cs; bb = col0 + i; }
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    const float cs = v[i] * inv_a * sm.inv[2 * (col0 + i) + 1];
+                    if (cs > best) { best = cs; bb = col0 + i; }
                 }
-                sm.best[half * 128 + a] = best;
-                sm.bestb[half * 128 + a] = bb;
+                sm.best[grp * 128 + a] = best;
+                sm.bestb[grp * 128 + a] = bb;
             }
             tc_fence_before();
             __syncthreads();
 
             // (4) selection, merge plan, compaction map
-            chunk_tables(sm, sN, c, m, 2);
+            chunk_tables(sm, sN, c, m, 4);
             if (p.match_out && tid < 128) p.match_out[((size_t)u * p.maxch + j) * 128 + tid] = sm.match[tid];
             if (j == 0 && tid == 0) p.len[u] = s - ch * m;
             if (tid == 0) poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
@@ -327,12 +328,12 @@ int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint6
         auto kern = csm_tc_kernel<128>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<128>::kSmem) != cudaSuccess)
             return CSMKV_ERR_CUDA;
-        kern<<<grid, kCsmThreads, TcRing<128>::kSmem, st>>>(P, tmK, tmV, tmN);
+        kern<<<grid, kTcThreads, TcRing<128>::kSmem, st>>>(P, tmK, tmV, tmN);
     } else {
         auto kern = csm_tc_kernel<64>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<64>::kSmem) != cudaSuccess)
             return CSMKV_ERR_CUDA;
-        kern<<<grid, kCsmThreads, TcRing<64>::kSmem, st>>>(P, tmK, tmV, tmN);
+        kern<<<grid, kTcThreads, TcRing<64>::kSmem, st>>>(P, tmK, tmV, tmN);
     }
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
 }
