@@ -176,6 +176,35 @@ int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t*
                      void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Decode attention without a caller-provided workspace.
+ * (The pages have no counterpart: this is a deployment convenience.)
+ *
+ * For callers that cannot allocate device memory -- code running after the
+ * host application has reserved all device memory, plugins that do not own
+ * the CUDA allocator, services whose memory budget is fixed before the first
+ * request. Same computation, arguments and layouts as decode_attn_logn, minus
+ * the workspace: the scratch is a fixed 16 MiB array inside the library, one
+ * per GPU that loads it, held until the process exits.
+ *  - Capacity: returns CSMKV_ERR_WORKSPACE when decode_attn_workspace_bytes(
+ *    cache, h_q) exceeds 16 MiB (at head_dim 128 on 152 SMs: about 700
+ *    (sequence, KV head) units). Nothing is launched then.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call zero-fills the part of the array it uses, asynchronously on
+ *    `stream`, then runs decode_attn_logn on it. The library allocates
+ *    nothing.
+ *  - All calls on a device share the one array: calls that overlap on the GPU
+ *    (different streams, no ordering between them) race and give wrong
+ *    results. Device-side errors are recorded in the array's status word and
+ *    cleared by the next call; use decode_attn_logn with a workspace when
+ *    they must be read back.
+ * ---------------------------------------------------------------------- */
+int decode_attn_logn_noalloc(const void* q, const void* K, const void* V, const int32_t* N,
+                             const int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale,
+                             void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Host-side schedule helpers   [Chelsea §三 算法流程, Algorithm 1;
  *                               CentroidKV 分块软匹配 (CSM), 渐进式调度]
  * Pure functions; no device work.

@@ -57,6 +57,7 @@ _SIGS = {
     "csm_append": (ctypes.c_int, [P, P, P, P, CP, P, P, P, P, SZ, P]),
     "decode_attn_workspace_bytes": (SZ, [CP, I32]),
     "decode_attn_logn": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
+    "decode_attn_logn_noalloc": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P]),
     "csm_budget": (F64, [I64, F64, I64]),
     "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
     "csm_ratio": (F64, [I32, F64, F64, F64]),
@@ -177,6 +178,18 @@ def decode_attn_logn(q, K, V, N, length, out, workspace, scale=None, stream=None
     rc = load().decode_attn_logn(_ptr(q), _ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), h_q,
                                  float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("decode_attn_logn", rc)
+
+
+def decode_attn_logn_noalloc(q, K, V, N, length, out, scale=None, stream=None):
+    """decode_attn_logn with the library's own fixed scratch instead of a workspace,
+    for callers that cannot allocate device memory."""
+    cache = cache_desc(K)
+    h_q = q.shape[1]
+    if scale is None:
+        scale = 1.0 / (K.shape[-1] ** 0.5)
+    rc = load().decode_attn_logn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache),
+                                         h_q, float(scale), _ptr(out), _stream(stream))
+    _check("decode_attn_logn_noalloc", rc)
 
 
 # ---------------------------------------------------------------- host helpers
