@@ -38,6 +38,9 @@ METRIC = "CSM KV tokens compressed/s; log-N decode-attn HBM GB/s (% of peak), 1Ã
 FALLBACK_HBM_GBS = 6800.0
 
 
+CSM_KERNELS = {"auto": 0, "simt": 1, "ring": 2, "split": 3}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -266,7 +269,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     d = synth.make_device(w)
     K0, V0, N0, L0 = (d[k].clone() for k in ("K", "V", "N", "len"))
-    p = Pipeline(w, d, stream=None)
+    p = Pipeline(w, d, stream=None, csm_kernel=CSM_KERNELS[args.csm_kernel])
     head_mask = d["head_mask"].cpu().numpy()
     rounds = p.rounds
 
@@ -356,7 +359,7 @@ def run_gpu(args):
     per_launch_bytes = attn_bytes_step / w.steps
     avg_launch_s = (attn_ms / 1e3) / max(1, attn_calls)
     csm_gbs = csm_bytes_step * args.steps / (csm_ms / 1e3) / 1e9
-    cpu = oracle_sample(w, units=args.ref_units) if not args.no_cpu_baseline else None
+    cpu = oracle_sample(w, units=args.cpu_units) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC,
         "value": agg["tokens"] / agg["csm_s"],
@@ -380,6 +383,7 @@ def run_gpu(args):
                      "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
         "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
                          "traffic": traffic_record("csm_compress.cu"), "kernel": "csm_compress",
+                         "csm_kernel": args.csm_kernel,
                          "peak_kind": kind, "bytes_per_step": csm_bytes_step},
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
                 "ms_per_step": csm_ms / args.steps, "rounds_per_step": len(rounds)},
@@ -472,7 +476,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="llama_64k_32l")
     ap.add_argument("--ref-units", type=int, default=16)
+    ap.add_argument("--cpu-units", type=int, default=256,
+                    help="(layer, KV head) units in the oracle's timed sample (about 10 s on 16 cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--csm-kernel", default="auto", choices=sorted(CSM_KERNELS),
+                    help="compression kernel: auto, simt (CUDA cores), ring or split (tensor cores)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

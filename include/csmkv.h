@@ -121,8 +121,18 @@ typedef struct {
                                  flags, so every wait on another item runs into the
                                  timeout and reports CSMKV_ERR_TIMEOUT (the cache is
                                  then partly compacted and must be discarded) */
-    int32_t force_simt;       /* 1 = use the CUDA-core similarity path everywhere */
+    int32_t kernel;           /* which compression kernel runs (CSM_KERNEL_*) */
 } csm_options;
+
+/* csm_options.kernel. AUTO picks a tensor-core kernel where the shape allows
+ * one (bf16, c == 256, head_dim in {64, 128}) and the CUDA-core kernel
+ * elsewhere; asking for a tensor-core kernel on another shape falls back to
+ * the CUDA-core kernel. All choices give the same decisions and outputs up to
+ * the order of fp32 rounding in the similarity scores. */
+#define CSM_KERNEL_AUTO 0
+#define CSM_KERNEL_SIMT 1    /* fp32 CUDA cores, one persistent CTA per SM */
+#define CSM_KERNEL_TC_RING 2 /* tcgen05, one CTA per SM with a 3-slot TMA ring */
+#define CSM_KERNEL_TC_SPLIT 3 /* tcgen05, three CTAs per SM with one slot each */
 
 /* csm_compress plus two optional outputs/controls:
  * match_out: device int32 [batch*h_kv][csm_max_chunks(...)][c/2] or NULL.

@@ -35,7 +35,10 @@ class Cache(ctypes.Structure):
 
 class CsmOptions(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("withhold_signals", ctypes.c_int32),
-                ("force_simt", ctypes.c_int32)]
+                ("kernel", ctypes.c_int32)]
+
+
+CSM_KERNEL_AUTO, CSM_KERNEL_SIMT, CSM_KERNEL_TC_RING, CSM_KERNEL_TC_SPLIT = 0, 1, 2, 3
 
 
 _lib = None
@@ -142,9 +145,9 @@ def csm_compress(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, w
 
 
 def csm_compress_ex(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, match_out=None,
-                    wait_timeout_ns=0, withhold_signals=0, force_simt=0, workspace=None, stream=None):
+                    wait_timeout_ns=0, withhold_signals=0, kernel=0, workspace=None, stream=None):
     cache = cache_desc(K)
-    opts = CsmOptions(int(wait_timeout_ns), int(withhold_signals), int(force_simt))
+    opts = CsmOptions(int(wait_timeout_ns), int(withhold_signals), int(kernel))
     rc = load().csm_compress_ex(_ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), n1, n2, c,
                                 float(r), _ptr(head_mask), _ptr(seq_mask), _ptr(match_out),
                                 ctypes.byref(opts), _ptr(workspace),

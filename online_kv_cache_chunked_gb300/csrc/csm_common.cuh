@@ -68,30 +68,38 @@ struct Elem<float> {
     }
 };
 
-// Shared-memory tables of one chunk's decisions.
-struct CsmTables {
-    float inv[256];       // inverse key norm per chunk row
-    float best[512];      // per-group best similarity, then final per A row
-    int32_t bestb[512];   // per-group argmax, then final per A row
-    int32_t match[128];   // B index for selected A rows, else -1
-    int32_t cnt[128];     // incoming edges per B row
-    int32_t off[128];     // CSR offsets per B row
-    int32_t nsum[128];    // merged degree per B row
-    float ninv[128];      // 1 / nsum
-    int32_t pre[132];     // selected A rows before index a (pre[H] = m)
-    int16_t src[256];     // output row -> chunk row
-    uint8_t list[128];    // CSR member list (A indices)
-    int32_t misc[8];      // [3..6] warp selection counts
+// Shared-memory tables of one chunk's decisions. 16-byte aligned and sized, so
+// whatever follows it in shared memory (mbarriers included) stays aligned.
+struct alignas(16) CsmTables {
+    float invA[128];        // inverse key norm of A row a (chunk offset 2a)
+    float invB[128];        // inverse key norm of B row b (chunk offset 2b+1)
+    float best[512];        // per-group best similarity, then final per A row
+    uint8_t bestb[512];     // per-group argmax, then final per A row
+    int16_t match[128];     // B index for selected A rows, else -1
+    uint32_t mask[128][4];  // bit a set: A row a merges into this B row
+    int32_t nsum[128];      // degree of B row b after the round
+    float ninv[128];        // 1 / nsum for B rows with incoming edges, 0 otherwise
+    int16_t pre[136];       // selected A rows before index a (pre[H] = m)
+    int16_t src[256];       // output row -> chunk row (only when m < H)
+    uint8_t mlist[128];     // B rows with incoming edges, ascending
+    int32_t nmerged;        // their count
+    int32_t misc[8];        // [3..6] warp counts
 };
+static_assert(sizeof(CsmTables) % 16 == 0, "tables keep what follows them aligned");
 
-// Non-empty work item at or after a ticket, or INT_MAX. Thread 0 only.
-__device__ __forceinline__ int claim_item(const CsmParams& p, int levels_ch, long long total) {
+// First non-empty work item at or after ticket t (claiming further tickets past
+// empty ones), or INT_MAX when the work is done or a CTA has failed.
+__device__ __forceinline__ int claim_from(const CsmParams& p, int t, int levels_ch, long long total) {
     for (;;) {
-        int t = atomicAdd(&p.hdr->ticket, 1);
         if (t >= total || ld_volatile(&p.hdr->status) != 0) return INT_MAX;
         const int lev = t / p.BH, u = t - lev * p.BH;
         if (lev < levels_ch ? lev < p.unit_ch[u] : (lev - levels_ch) < p.unit_tp[u]) return t;
+        t = atomicAdd(&p.hdr->ticket, 1);
     }
+}
+
+__device__ __forceinline__ int claim_item(const CsmParams& p, int levels_ch, long long total) {
+    return claim_from(p, atomicAdd(&p.hdr->ticket, 1), levels_ch, total);
 }
 
 // Bounded wait by thread 0 on a run of item flags; the result is broadcast to the block.
@@ -110,12 +118,16 @@ __device__ __forceinline__ void publish(int32_t* flag, int32_t epoch, int withho
 }
 
 // From per-group (best, argmax) records to the chunk's merge plan: exactly m
-// selected A rows (similarity desc, A index asc), the output row -> chunk row
-// map, and the CSR list of A rows merging into every B row. All threads call.
+// selected A rows (similarity desc, A index asc), for every B row the set of A
+// rows merging into it (a bit mask: atomicOr makes it independent of thread
+// order, so the merge sums run in A order on every run), the merged degrees and,
+// when m < H, the output row -> chunk row map. With m == H every A row is
+// selected and the output rows are exactly the B rows. All threads call.
 // With H = 128 and 256 or 512 threads, R = blockDim / 128 consecutive threads
-// share one A row's rank count and list position.
+// share one A row's rank count.
 __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int m, int ngroups) {
     const int H = c / 2;
+    const bool all = (m == H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = (H == 128 && blockDim.x >= 256) ? (int)blockDim.x / 128 : 1;  // 1, 2 or 4
     const int ra = tid / R, rp = tid - ra * R, span = H / R;
@@ -127,11 +139,17 @@ __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int
             if (v > best) { best = v; bb = sm.bestb[g * H + tid]; }
         }
         sm.best[tid] = (best == best) ? best : -INFINITY;  // a NaN key ranks last
-        sm.bestb[tid] = bb;
-        sm.cnt[tid] = 0;
+        sm.bestb[tid] = (uint8_t)bb;
+        sm.mask[tid][0] = sm.mask[tid][1] = sm.mask[tid][2] = sm.mask[tid][3] = 0u;
     }
     __syncthreads();
-    if (ra < H) {  // rank of A row ra among all A rows, counted over R parts
+    if (all) {
+        if (tid < H) {
+            const int b = sm.bestb[tid];
+            sm.match[tid] = (int16_t)b;
+            atomicOr(&sm.mask[b][tid >> 5], 1u << (tid & 31));
+        }
+    } else if (ra < H) {  // rank of A row ra among all A rows, counted over R parts
         const float key = sm.best[ra];
         int rank = 0;
         const int a0 = rp * span;
@@ -144,118 +162,115 @@ __device__ inline void chunk_tables(CsmTables& sm, const int32_t* sN, int c, int
         for (int o = 1; o < R; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
         if (rp == 0) {
             const bool sel = rank < m;
-            sm.match[ra] = sel ? sm.bestb[ra] : -1;
-            if (sel) atomicAdd(&sm.cnt[sm.bestb[ra]], 1);
+            const int b = sm.bestb[ra];
+            sm.match[ra] = (int16_t)(sel ? b : -1);
+            if (sel) atomicOr(&sm.mask[b][ra >> 5], 1u << (ra & 31));
         }
     }
     __syncthreads();
-    const bool sel = tid < H && sm.match[tid] >= 0;
-    {   // exclusive prefix of the selection over A (H <= 128 -> warps 0..3)
+    if (!all) {  // exclusive prefix of the selection over A (H <= 128 -> warps 0..3)
+        const bool sel = tid < H && sm.match[tid] >= 0;
         const unsigned bal = __ballot_sync(0xffffffffu, sel);
         if (lane == 0 && warp < 4) sm.misc[3 + warp] = __popc(bal);
         __syncthreads();
         if (tid < H) {
             int before = __popc(bal & ((1u << lane) - 1u));
             for (int w = 0; w < warp; ++w) before += sm.misc[3 + w];
-            sm.pre[tid] = before;
+            sm.pre[tid] = (int16_t)before;
         }
-        if (tid == 0) sm.pre[H] = m;
-    }
-    if (warp == 0) {  // CSR offsets of incoming edges per B row (H <= 128: 4 per lane)
-        int v[4], run = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int b = lane * 4 + i;
-            v[i] = b < H ? sm.cnt[b] : 0;
-            run += v[i];
-        }
-        int incl = run;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
-        }
-        int ex = incl - run;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int b = lane * 4 + i;
-            if (b < H) sm.off[b] = ex;
-            ex += v[i];
+        if (tid == 0) sm.pre[H] = (int16_t)m;
+        __syncthreads();
+        for (int q = tid; q < c; q += blockDim.x) {
+            if ((q & 1) == 0) {
+                if (sm.match[q >> 1] < 0) sm.src[q - sm.pre[q >> 1]] = (int16_t)q;
+            } else {
+                sm.src[q - sm.pre[(q >> 1) + 1]] = (int16_t)q;
+            }
         }
     }
-    __syncthreads();
-    for (int q = tid; q < c; q += blockDim.x) {
-        if ((q & 1) == 0) {
-            if (sm.match[q >> 1] < 0) sm.src[q - sm.pre[q >> 1]] = (int16_t)q;
-        } else {
-            sm.src[q - sm.pre[(q >> 1) + 1]] = (int16_t)q;
-        }
-    }
-    if (ra < H) {  // position of a selected A row in its target's list: earlier A rows with the same target
-        const int b = sm.match[ra];
-        int r = 0;
-        if (b >= 0) {
-            const int a0 = rp * span, a1 = min(a0 + span, ra);
-            for (int a2 = a0; a2 < a1; ++a2) r += (sm.match[a2] == b);
-        }
-        for (int o = 1; o < R; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-        if (b >= 0 && rp == 0) sm.list[sm.off[b] + r] = (uint8_t)ra;
-    }
-    __syncthreads();
     if (tid < H) {
         int ns = sN[2 * tid + 1];
-        const int o0 = sm.off[tid], o1 = o0 + sm.cnt[tid];
-        for (int k = o0; k < o1; ++k) ns += sN[2 * (int)sm.list[k]];
+        bool any = false;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t bits = sm.mask[tid][w];
+            any |= bits != 0u;
+            while (bits) {
+                ns += sN[2 * (w * 32 + __ffs(bits) - 1)];
+                bits &= bits - 1u;
+            }
+        }
         sm.nsum[tid] = ns;
-        sm.ninv[tid] = 1.0f / (float)ns;
+        sm.ninv[tid] = any ? 1.0f / (float)ns : 0.0f;
+    }
+    {   // list of the merged B rows (H <= 128 -> warps 0..3)
+        const bool any = tid < H && sm.ninv[tid] != 0.0f;
+        const unsigned bal = __ballot_sync(0xffffffffu, any);
+        __syncthreads();  // misc is reused; also orders the ninv writes above
+        if (lane == 0 && warp < 4) sm.misc[3 + warp] = __popc(bal);
+        __syncthreads();
+        if (any) {
+            int pos = __popc(bal & ((1u << lane) - 1u));
+            for (int w = 0; w < warp; ++w) pos += sm.misc[3 + w];
+            sm.mlist[pos] = (uint8_t)tid;
+        }
+        if (tid == 0) sm.nmerged = sm.misc[3] + sm.misc[4] + sm.misc[5] + sm.misc[6];
     }
     __syncthreads();
 }
 
 // Writes the c - m output rows of one array of a chunk: copies, or degree-
-// weighted means for B rows with incoming edges (fp32 sums scaled by the reciprocal
-// of the degree sum, rounded once to the cache dtype).
+// weighted means for B rows with incoming edges (fp32 sums in A order, scaled
+// by the reciprocal of the degree sum, rounded once to the cache dtype).
 // piece(q, cc) gives the 16-byte piece cc of chunk row q in shared memory.
 template <typename T, typename PieceFn>
-__device__ __forceinline__ void emit_rows(T* dst_rows, int rows_out, int D, const CsmTables& sm,
+__device__ __forceinline__ void emit_rows(T* dst_rows, int rows_out, int D, int m, const CsmTables& sm,
                                           const int32_t* sN, PieceFn piece) {
     using E = Elem<T>;
     constexpr int EPP = E::kPer;
     const int PR = D * (int)sizeof(T) / 16;
+    const bool all = (rows_out == m);  // c - m == m exactly when m == H: the output rows are the B rows
     const int npieces = rows_out * PR;
     for (int i = threadIdx.x; i < npieces; i += blockDim.x) {
         const int pr = i / PR, cc = i - pr * PR;
-        const int q = sm.src[pr];
-        uint4 val;
-        if ((q & 1) && sm.cnt[q >> 1] > 0) {
+        const int q = all ? 2 * pr + 1 : sm.src[pr];
+        uint4 val = *reinterpret_cast<const uint4*>(piece(q, cc));
+        if (q & 1) {
             const int b = q >> 1;
-            float acc[EPP], f[EPP];
-            E::unpack(*reinterpret_cast<const uint4*>(piece(q, cc)), f);
-            const float nb = (float)sN[q];
+            const float inv = sm.ninv[b];
+            if (inv != 0.0f) {
+                float acc[EPP], f[EPP];
+                E::unpack(val, f);
+                const float nb = (float)sN[q];
 #pragma unroll
-            for (int e = 0; e < EPP; ++e) acc[e] = nb * f[e];
-            const int o0 = sm.off[b], o1 = o0 + sm.cnt[b];
-            for (int k = o0; k < o1; ++k) {
-                const int qa = 2 * (int)sm.list[k];
-                E::unpack(*reinterpret_cast<const uint4*>(piece(qa, cc)), f);
-                const float na = (float)sN[qa];
+                for (int e = 0; e < EPP; ++e) acc[e] = nb * f[e];
 #pragma unroll
-                for (int e = 0; e < EPP; ++e) acc[e] = fmaf(na, f[e], acc[e]);
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t bits = sm.mask[b][w];
+                    while (bits) {
+                        const int qa = 2 * (w * 32 + __ffs(bits) - 1);
+                        bits &= bits - 1u;
+                        E::unpack(*reinterpret_cast<const uint4*>(piece(qa, cc)), f);
+                        const float na = (float)sN[qa];
+#pragma unroll
+                        for (int e = 0; e < EPP; ++e) acc[e] = fmaf(na, f[e], acc[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < EPP; ++e) acc[e] *= inv;
+                val = E::pack(acc);
             }
-            const float inv = sm.ninv[b];  // one reciprocal per merged row
-#pragma unroll
-            for (int e = 0; e < EPP; ++e) acc[e] *= inv;
-            val = E::pack(acc);
-        } else {
-            val = *reinterpret_cast<const uint4*>(piece(q, cc));
         }
         *reinterpret_cast<uint4*>(dst_rows + (size_t)pr * D + cc * EPP) = val;
     }
 }
 
-__device__ __forceinline__ void emit_degrees(int32_t* dstN, int rows_out, const CsmTables& sm, const int32_t* sN) {
+__device__ __forceinline__ void emit_degrees(int32_t* dstN, int rows_out, int m, const CsmTables& sm,
+                                             const int32_t* sN) {
+    const bool all = (rows_out == m);
     for (int pr = threadIdx.x; pr < rows_out; pr += blockDim.x) {
-        const int q = sm.src[pr];
-        dstN[pr] = ((q & 1) && sm.cnt[q >> 1] > 0) ? sm.nsum[q >> 1] : sN[q];
+        const int q = all ? 2 * pr + 1 : sm.src[pr];
+        dstN[pr] = (q & 1) ? sm.nsum[q >> 1] : sN[q];
     }
 }
 
@@ -326,7 +341,9 @@ __device__ bool tail_piece(const CsmParams& p, int u, int piece, int32_t epoch, 
     return true;
 }
 
-// Tensor-core path launcher (csm_tc.cu).
+// Tensor-core launchers: one persistent CTA per SM with a TMA ring (csm_tc.cu),
+// three CTAs per SM with one slot each (csm_tc3.cu).
+int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st);
 int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st);
 
 }  // namespace csmkv

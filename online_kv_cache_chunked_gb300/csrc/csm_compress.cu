@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kCsmThreads, 1) csm_simt_kernel(const CsmParam
 #pragma unroll
                     for (int e = 0; e < EPP; ++e) ss = fmaf(f[e], f[e], ss);
                 }
-                sm.inv[q] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
+                const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
+                if (q & 1) sm.invB[q >> 1] = inv; else sm.invA[q >> 1] = inv;
             }
             __syncthreads();
             // groups of B columns per A row; a later group wins only if strictly better
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kCsmThreads, 1) csm_simt_kernel(const CsmParam
                 const int a = tid % H, g = tid / H;
                 if (g < ngroups) {
                     const int b0 = g * per, b1 = min(H, b0 + per);
-                    const float inv_a = sm.inv[2 * a];
+                    const float inv_a = sm.invA[a];
                     float best = -INFINITY;
                     int bb = b0;
                     for (int b = b0; b < b1; ++b) {
@@ -152,16 +153,16 @@ __global__ void __launch_bounds__(kCsmThreads, 1) csm_simt_kernel(const CsmParam
 #pragma unroll
                             for (int e = 0; e < EPP; ++e) dot = fmaf(fa[e], fb[e], dot);
                         }
-                        const float cs = dot * inv_a * sm.inv[2 * b + 1];
+                        const float cs = dot * inv_a * sm.invB[b];
                         if (cs > best) { best = cs; bb = b; }
                     }
                     sm.best[g * H + a] = best;
-                    sm.bestb[g * H + a] = bb;
+                    sm.bestb[g * H + a] = (uint8_t)bb;
                 }
             }
             __syncthreads();
             chunk_tables(sm, sN, c, m, ngroups);
-            if (p.match_out && tid < H) p.match_out[((size_t)u * p.maxch + j) * H + tid] = sm.match[tid];
+            if (p.match_out && tid < H) p.match_out[((size_t)u * p.maxch + j) * H + tid] = (int32_t)sm.match[tid];
             if (j == 0 && tid == 0) p.len[u] = s - ch * m;
             int lo, hi;
             chunk_deps(j, c, m, lo, hi);
@@ -169,8 +170,8 @@ __global__ void __launch_bounds__(kCsmThreads, 1) csm_simt_kernel(const CsmParam
                 record_status(status, CSMKV_ERR_TIMEOUT);
                 break;
             }
-            emit_rows<T>(Kg + (urow + dst_row) * D, c - m, D, sm, sN, piece);
-            emit_degrees(p.N + urow + dst_row, c - m, sm, sN);
+            emit_rows<T>(Kg + (urow + dst_row) * D, c - m, D, m, sm, sN, piece);
+            emit_degrees(p.N + urow + dst_row, c - m, m, sm, sN);
             __syncthreads();
             stage_rows(Vg);
             __syncthreads();
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kCsmThreads, 1) csm_simt_kernel(const CsmParam
                 record_status(status, CSMKV_ERR_TIMEOUT);
                 break;
             }
-            emit_rows<T>(Vg + (urow + dst_row) * D, c - m, D, sm, sN, piece);
+            emit_rows<T>(Vg + (urow + dst_row) * D, c - m, D, m, sm, sN, piece);
         } else if (!tail_piece<T>(p, u, lev - levels_ch, epoch, stage, sN)) {
             record_status(status, CSMKV_ERR_TIMEOUT);
             break;
@@ -280,8 +281,12 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
 
     const int D = cache->head_dim;
-    const bool tc = cache->dtype == CSMKV_BF16 && c == 256 && (D == 64 || D == 128) && !(opts && opts->force_simt);
-    if (tc) return launch_csm_tc(P, D, K, V, N, (uint64_t)cache->batch * cache->h_kv * cache->cap, st);
+    const int want = opts ? opts->kernel : CSM_KERNEL_AUTO;
+    if (want < CSM_KERNEL_AUTO || want > CSM_KERNEL_TC_SPLIT) return CSMKV_ERR_ARG;
+    const bool tc = cache->dtype == CSMKV_BF16 && c == 256 && (D == 64 || D == 128) && want != CSM_KERNEL_SIMT;
+    const uint64_t rows = (uint64_t)cache->batch * cache->h_kv * cache->cap;
+    if (tc && want == CSM_KERNEL_TC_RING) return launch_csm_tc(P, D, K, V, N, rows, st);
+    if (tc) return launch_csm_tc3(P, D, K, V, N, rows, st);
     const int RB = D * (int)dtype_bytes(cache->dtype);
     const int smem = csm_stage_bytes_simt(c, RB) + (int)sizeof(CsmTables) + 257 * 4 + 1024;
     if (smem > 227 * 1024) return CSMKV_ERR_UNSUPPORTED;

@@ -20,6 +20,20 @@
 
 namespace csmkv {
 
+constexpr int kTcThreads = 512;  // 16 warps: 4 TMEM lane quarters x 4 column groups
+
+struct alignas(16) TcState {
+    uint64_t bar[3];  // one per ring slot
+    uint64_t mma_bar;
+    int32_t tk[3];    // tickets: current item, next, the one after
+    uint32_t tmem;
+    int32_t raw_tk;   // ticket fetched early in the iteration, checked at its end
+    int32_t raw_ok;   // that ticket is a non-empty item
+    int32_t mma_early;  // the MMA of the next item was issued at the end of this one
+    int32_t defer_k;    // chunk whose K load waits for the last V store to leave its slot
+    int32_t dep_ok[2];  // flags this chunk waits on were already set (K+N, V)
+};
+
 template <int D>
 struct TcRing {
     static constexpr int kBoxes = D / 64;
@@ -28,22 +42,15 @@ struct TcRing {
     static constexpr int kNRows = 65;                      // degree tile: 65 x 4 int32 covers 256 rows
     static constexpr int kNBytes = kNRows * 16;
     static constexpr int kNStride = 1152;                  // per-slot degree buffer
-    static constexpr int kSmem = kSlots * kSlotBytes + kSlots * kNStride + (int)sizeof(CsmTables) + 64 + 1024;
-};
-
-constexpr int kTcThreads = 512;  // 16 warps: 4 TMEM lane quarters x 4 column groups
-
-struct TcState {
-    uint64_t bar[3];  // one per ring slot
-    uint64_t mma_bar;
-    int32_t tk[3];    // tickets: current item, next, the one after
-    uint32_t tmem;
+    static constexpr int kSmem = kSlots * kSlotBytes + kSlots * kNStride + (int)sizeof(CsmTables) + (int)sizeof(TcState) + 1024;
+    static_assert((kSlots * kSlotBytes + kSlots * kNStride) % 16 == 0, "tables start 16-byte aligned");
 };
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     csm_tc_kernel(const __grid_constant__ CsmParams p, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN,
+                  const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs) {
     using R = TcRing<D>;
     using T = __nv_bfloat16;
     extern __shared__ uint8_t smem_raw[];
@@ -60,12 +67,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int32_t* const status = &p.hdr->status;
 
     if (tid == 0) {
+        bulk_wait_all();  // output stores complete before the CTA exits
         for (int s = 0; s < R::kSlots; ++s) mbar_init(&st.bar[s], 1);
         mbar_init(&st.mma_bar, 1);
         fence_mbar_init();
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmN);
+        prefetch_tmap(&tmKs);
+        prefetch_tmap(&tmVs);
+        st.mma_early = 0;
+        st.defer_k = INT_MAX;
     }
     if (warp == 0) {
         tmem_alloc(&st.tmem, 128);
@@ -76,6 +88,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = st.tmem;
 
     const int32_t epoch = p.hdr->epoch;
+    const bool all = (m == 128);  // every A row merges: the output rows are the B rows, in order
+    bool stores_pending = false;  // thread 0: TMA stores committed since the last read-wait
     const int levels_ch = p.hdr->levels_ch, levels_tail = p.hdr->levels_tail;
     const long long total = (long long)(levels_ch + levels_tail) * BH;
 
@@ -116,13 +130,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         pend_bits |= 1u << slot;
     };
-    // Thread 0: publish a prefetched item's flag as soon as its slot has landed.
+    // Flags are published by one thread that writes no global memory on the m == H
+    // path, so its release stores never wait behind output writes. Polling a slot
+    // whose load is not issued yet finds its next phase incomplete and does nothing.
+    const bool publisher = (tid == 256);
     auto poll_publish = [&](int t, int slot, int32_t* flags_base, bool& done) {
-        if (done || !is_chunk(t) || !((pend_bits >> slot) & 1u)) return;
-        if (mbar_try_wait(&st.bar[slot], ((phase_bits >> slot) & 1u))) {
+        if (done || !is_chunk(t)) return;
+        if (mbar_test(&st.bar[slot], ((phase_bits >> slot) & 1u))) {
             const int j = t / BH, u = t - j * BH;
             publish(flags_base + (size_t)u * p.L + j, epoch, p.withhold);
             done = true;
+        }
+    };
+
+    // m == H: every merged B row replaces its own shared-memory row (same arithmetic
+    // as emit_rows: fp32 sums in A order, scaled by 1 / degree sum, rounded once).
+    auto merge_inplace = [&](auto piece, const int32_t* sN) {
+        constexpr int PR = D / 8;
+        const int n = sm.nmerged * PR;
+        for (int i = tid; i < n; i += kTcThreads) {
+            const int k = i / PR, cc = i - k * PR;
+            const int b = sm.mlist[k], q = 2 * b + 1;
+            uint4* dst = reinterpret_cast<uint4*>(piece(q, cc));
+            float acc[8], f[8];
+            Elem<T>::unpack(*dst, f);
+            const float nb = (float)sN[q];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = nb * f[e];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t bits = sm.mask[b][w];
+                while (bits) {
+                    const int qa = 2 * (w * 32 + __ffs(bits) - 1);
+                    bits &= bits - 1u;
+                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(piece(qa, cc)), f);
+                    const float na = (float)sN[qa];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(na, f[e], acc[e]);
+                }
+            }
+            const float inv = sm.ninv[b];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= inv;
+            *dst = Elem<T>::pack(acc);
         }
     };
 
@@ -148,6 +198,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool kn_done_now = kn_next_done, v_done_now = v_next_done;
         kn_next_done = v_next_done = false;
         bool ok = true;
+        // Off the critical path: thread 32 fetches the ticket after next and thread 64
+        // peeks at the flags this chunk will wait on; both results are used much later.
+        int raw_ticket = INT_MAX, raw_uch = 0;
+        if (tid == 32) raw_ticket = atomicAdd(&p.hdr->ticket, 1);
+        // relaxed loads of at most two K and two V flags; compared (and fenced) later
+        int32_t pk0 = epoch, pk1 = epoch, pv0 = epoch, pv1 = epoch;
+        if (tid == 64 && lev < levels_ch) {
+            int lo, hi;
+            chunk_deps(lev, c, p.m, lo, hi);
+            const int32_t* fk = p.flag_kn + (size_t)u * p.L;
+            const int32_t* fw = p.flag_v + (size_t)u * p.L;
+            if (lo <= hi) {
+                pk0 = ld_volatile(fk + lo);
+                pv0 = ld_volatile(fw + lo);
+            }
+            if (lo < hi) {
+                pk1 = ld_volatile(fk + hi);
+                pv1 = ld_volatile(fw + hi);
+            }
+        }
 
         if (lev < levels_ch) {
             // ================================================================ chunk item
@@ -175,27 +245,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
             if (tid == 0) {
                 pend_bits &= ~(1u << kslot);
-                if (!kn_done_now) publish(fkn + j, epoch, p.withhold);
-            }
-
-            // (2) inverse key norms, two threads per chunk row (c = 256 rows, 512 threads)
-            {
-                const int q = tid >> 1, h = tid & 1;
-                float ss = 0.f;
-#pragma unroll
-                for (int i = 0; i < D / 16; ++i) {
-                    float f[8];
-                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(kpiece(q, h * (D / 16) + i)), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                if (st.defer_k != INT_MAX) {  // K two items ahead, once the last V store left its slot
+                    bulk_wait_read_all();
+                    stores_pending = false;
+                    issue_k(st.defer_k, nkslot);
+                    st.defer_k = INT_MAX;
                 }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (h == 0) sm.inv[q] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
             }
-            __syncthreads();
-
-            // (3) 128 x 128 dot products on the tensor cores, read back by 8 warps
-            if (tid == 0) {
+            if (publisher && !kn_done_now) publish(fkn + j, epoch, p.withhold);
+            // (2) the 128 x 128 dot products start on the tensor cores now; the norms
+            // below run on the CUDA cores meanwhile
+            if (tid == 0 && !st.mma_early) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -206,8 +266,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_commit(&st.mma_bar);
                 mma_pend = true;
-                poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
             }
+            if (publisher) poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
+
+            // (2b) inverse key norms, two threads per chunk row. A quarter warp covers 8
+            // consecutive rows of one operand, reading physical 16-byte chunks in swizzled
+            // order, so its loads hit distinct banks; the row's two halves meet by shuffle.
+            {
+                const int h = (tid >> 3) & 1, op = (tid >> 4) & 1;
+                const int idx = (tid & 7) | ((tid >> 5) << 3);  // row within its operand
+                const uint8_t* row = kb + op * R::kBoxes * 16384 + idx * 128;
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int box = R::kBoxes == 2 ? h : 0;
+                    const int chk = R::kBoxes == 2 ? i : (h * 4 + (i & 3));
+                    if (R::kBoxes == 1 && i >= 4) break;
+                    float f[8];
+                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(row + box * 16384 + ((chk ^ (idx & 7)) << 4)), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+                if (h == 0) {
+                    const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.0f;
+                    if (op) sm.invB[idx] = inv; else sm.invA[idx] = inv;
+                }
+                if (tid == 32) raw_uch = raw_ticket < total ? (raw_ticket / BH < levels_ch ? p.unit_ch[raw_ticket % BH]
+                                                                                          : p.unit_tp[raw_ticket % BH])
+                                                             : 0;
+                if (tid == 64) {
+                    const int ok_k = pk0 == epoch && pk1 == epoch, ok_v = pv0 == epoch && pv1 == epoch;
+                    if (ok_k || ok_v) __threadfence();  // acquire side of the flags seen set
+                    st.dep_ok[0] = ok_k;
+                    st.dep_ok[1] = ok_v;
+                }
+            }
+            __syncthreads();
+
+            // (3) the dot products, read back by 16 warps
             ok = mbar_wait(&st.mma_bar, mma_phase, globaltimer() + p.timeout_ns);
             mma_phase ^= 1u;
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
@@ -219,56 +316,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int col0 = grp * 32;
                 float v[32];
                 tmem_ld_32x32b_x32(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)col0, v);
-                const float inv_a = sm.inv[2 * a];
+                // argmax_b of dot * invB[b] (invA[a] > 0 does not move it), scaled once
+                const float inv_a = sm.invA[a];
+                const float4* ib = reinterpret_cast<const float4*>(sm.invB + col0);
                 float best = -INFINITY;
                 int bb = col0;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float cs = v[i] * inv_a * sm.inv[2 * (col0 + i) + 1];
-                    if (cs > best) { best = cs; bb = col0 + i; }
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 w4 = ib[i4];
+                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float cs = v[4 * i4 + e] * wv[e];
+                        if (cs > best) { best = cs; bb = col0 + 4 * i4 + e; }
+                    }
                 }
-                sm.best[grp * 128 + a] = best;
-                sm.bestb[grp * 128 + a] = bb;
+                if (inv_a == 0.0f) {  // a zero key has cosine 0 to every B row: lowest index
+                    best = 0.0f;
+                    bb = col0;
+                }
+                sm.best[grp * 128 + a] = best * inv_a;
+                sm.bestb[grp * 128 + a] = (uint8_t)bb;
             }
             tc_fence_before();
             __syncthreads();
 
             // (4) selection, merge plan, compaction map
             chunk_tables(sm, sN, c, m, 4);
-            if (p.match_out && tid < 128) p.match_out[((size_t)u * p.maxch + j) * 128 + tid] = sm.match[tid];
+            if (p.match_out && tid < 128) p.match_out[((size_t)u * p.maxch + j) * 128 + tid] = (int32_t)sm.match[tid];
             if (j == 0 && tid == 0) p.len[u] = s - ch * m;
-            if (tid == 0) poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
+            if (publisher) poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
 
             // (5) K and degrees: wait for the items whose sources we overwrite, then write
             int lo, hi;
             chunk_deps(j, c, m, lo, hi);
-            if (!wait_items(fkn, lo, hi, epoch, globaltimer() + p.timeout_ns)) {
+            if (!st.dep_ok[0] && !wait_items(fkn, lo, hi, epoch, globaltimer() + p.timeout_ns)) {
                 record_status(status, CSMKV_ERR_TIMEOUT);
                 break;
             }
-            emit_rows<T>(Kg + (urow + dst_row) * D, c - m, D, sm, sN, kpiece);
-            emit_degrees(p.N + urow + dst_row, c - m, sm, sN);
+            if (all) {  // merged B rows in place, then the B boxes go out by TMA
+                merge_inplace(kpiece, sN);
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+#pragma unroll
+                    for (int bx = 0; bx < R::kBoxes; ++bx)
+                        tma_store_2d(&tmKs, kb + (R::kBoxes + bx) * 16384, bx * 64, (int)(urow + dst_row));
+                    bulk_commit();
+                    stores_pending = true;
+                }
+            } else {
+                emit_rows<T>(Kg + (urow + dst_row) * D, c - m, D, m, sm, sN, kpiece);
+            }
+            emit_degrees(p.N + urow + dst_row, c - m, m, sm, sN);
 
             // (6) K's slot is free: start V of the next item there
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0 && is_chunk(tn)) issue_v(tn, kslot);
+            if (tid == 0 && is_chunk(tn) && !all) issue_v(tn, kslot);  // m == H: after the V store, below
 
             // (7) V on chip, publish, wait, write
             ok = mbar_wait(&st.bar[vslot], ((phase_bits >> vslot) & 1u), globaltimer() + p.timeout_ns);
             phase_bits ^= 1u << vslot;
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
-            if (tid == 0) {
-                pend_bits &= ~(1u << vslot);
+            if (tid == 0) pend_bits &= ~(1u << vslot);
+            if (publisher) {
                 if (!v_done_now) publish(fv + j, epoch, p.withhold);
                 poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
             }
-            if (!wait_items(fv, lo, hi, epoch, globaltimer() + p.timeout_ns)) {
+            if (!st.dep_ok[1] && !wait_items(fv, lo, hi, epoch, globaltimer() + p.timeout_ns)) {
                 record_status(status, CSMKV_ERR_TIMEOUT);
                 break;
             }
-            emit_rows<T>(Vg + (urow + dst_row) * D, c - m, D, sm, sN, vpiece);
-            if (tid == 0) {
+            if (all) {
+                merge_inplace(vpiece, sN);
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+#pragma unroll
+                    for (int bx = 0; bx < R::kBoxes; ++bx)
+                        tma_store_2d(&tmVs, vb + (R::kBoxes + bx) * 16384, bx * 64, (int)(urow + dst_row));
+                    bulk_commit();
+                    stores_pending = true;
+                    if (is_chunk(tn)) {  // K's slot is free once the K store has read it
+                        bulk_wait_read_but_one();
+                        issue_v(tn, kslot);
+                    }
+                }
+            } else {
+                emit_rows<T>(Vg + (urow + dst_row) * D, c - m, D, m, sm, sN, vpiece);
+            }
+            if (publisher) {
                 poll_publish(tn, nkslot, p.flag_kn, kn_next_done);
                 poll_publish(tn, kslot, p.flag_v, v_next_done);
             }
@@ -279,15 +417,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0 && is_chunk(tn)) issue_v(tn, kslot);
+            if (tid == 0) {
+                if (stores_pending) {
+                    bulk_wait_read_all();
+                    stores_pending = false;
+                }
+                if (st.defer_k != INT_MAX) {
+                    issue_k(st.defer_k, nkslot);
+                    st.defer_k = INT_MAX;
+                }
+                if (is_chunk(tn)) issue_v(tn, kslot);
+            }
         }
 
         // (8) V's slot is free: claim the item after next and start its K there
         fence_proxy_async_smem();
+        if (tid == 32) {
+            st.raw_tk = raw_ticket;
+            st.raw_ok = raw_uch > (raw_ticket / BH < levels_ch ? raw_ticket / BH : raw_ticket / BH - levels_ch);
+        }
         __syncthreads();
         if (tid == 0) {
-            const int t2 = claim_item(p, levels_ch, total);
-            if (is_chunk(t2)) issue_k(t2, vslot);
+            const int t2 = (st.raw_ok && ld_volatile(status) == 0) ? st.raw_tk : claim_from(p, st.raw_tk, levels_ch, total);
+            if (is_chunk(t2)) {
+                if (stores_pending) st.defer_k = t2;  // the V store may still be reading this slot
+                else issue_k(t2, vslot);
+            }
+            // the next chunk's MMA can start now if its K has landed (TMEM is free)
+            st.mma_early = 0;
+            if (is_chunk(tn) && mbar_test(&st.bar[nkslot], (phase_bits >> nkslot) & 1u)) {
+                const uint8_t* nkb = ring + nkslot * R::kSlotBytes;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int box = ks >> 2, koff = (ks & 3) * 32;
+                    const uint64_t ad = smem_desc_sw128(smem_u32(nkb + box * 16384 + koff));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(nkb + (R::kBoxes + box) * 16384 + koff));
+                    tc_mma_bf16(tmem, ad, bd, idesc_bf16_f32(128, 128), ks > 0 ? 1u : 0u);
+                }
+                tc_commit(&st.mma_bar);
+                mma_pend = true;
+                st.mma_early = 1;
+            }
             st.tk[0] = tn;
             st.tk[1] = t2;
         }
@@ -318,6 +489,13 @@ int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint6
     const uint64_t ndims[2] = {4, rows / 4};
     const uint64_t nstr[1] = {16};
     const uint32_t nbox[2] = {4, (uint32_t)TcRing<128>::kNRows};
+    CUtensorMap tmKs{}, tmVs{};
+    const uint64_t sdims[2] = {(uint64_t)D, rows};
+    const uint64_t sstr[1] = {(uint64_t)D * 2};
+    const uint32_t sbox[2] = {64, 128};
+    if (!encode_tiled(&tmKs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tmVs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return CSMKV_ERR_CUDA;
     if (!encode_tiled(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled(&tmN, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, N, ndims, nstr, nbox, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -328,12 +506,12 @@ int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint6
         auto kern = csm_tc_kernel<128>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<128>::kSmem) != cudaSuccess)
             return CSMKV_ERR_CUDA;
-        kern<<<grid, kTcThreads, TcRing<128>::kSmem, st>>>(P, tmK, tmV, tmN);
+        kern<<<grid, kTcThreads, TcRing<128>::kSmem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
     } else {
         auto kern = csm_tc_kernel<64>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<64>::kSmem) != cudaSuccess)
             return CSMKV_ERR_CUDA;
-        kern<<<grid, kTcThreads, TcRing<64>::kSmem, st>>>(P, tmK, tmV, tmN);
+        kern<<<grid, kTcThreads, TcRing<64>::kSmem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
     }
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
 }

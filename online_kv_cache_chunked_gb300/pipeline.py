@@ -93,10 +93,11 @@ class Pipeline:
     attention output of decode step i lands in self.out[i].
     """
 
-    def __init__(self, w, data, stream=None):
+    def __init__(self, w, data, stream=None, csm_kernel=B.CSM_KERNEL_AUTO):
         self.w = w
         self.d = data
         self.stream = stream
+        self.csm_kernel = int(csm_kernel)
         self.rounds = plan(w)
         K = data["K"]
         dev = K.device
@@ -128,8 +129,12 @@ class Pipeline:
             rd = self.rounds[k]
             if hook:
                 hook("csm", rd, True)
-            B.csm_compress(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
-                           self.masks[k], self.ws_csm, self.stream)
+            if self.csm_kernel == B.CSM_KERNEL_AUTO:
+                B.csm_compress(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
+                               self.masks[k], self.ws_csm, self.stream)
+            else:
+                B.csm_compress_ex(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
+                                  self.masks[k], kernel=self.csm_kernel, workspace=self.ws_csm, stream=self.stream)
             if hook:
                 hook("csm", rd, False)
 

@@ -30,7 +30,7 @@ def skip_vector(batch, h_kv, head_mask=None, seq_mask=None):
     return sk
 
 
-def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, force_simt=0, ws=None):
+def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, kernel=0, ws=None):
     cache = B.cache_desc(K)
     maxch = max(1, B.csm_max_chunks(cache, n1, n2, c))
     match = torch.full((K.shape[0] * K.shape[1], maxch, c // 2), -2, dtype=torch.int32, device=K.device)
@@ -39,18 +39,18 @@ def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, force_sim
     hm = None if head_mask is None else torch.as_tensor(np.asarray(head_mask, np.uint8)).to(K.device)
     sm = None if seq_mask is None else torch.as_tensor(np.asarray(seq_mask, np.uint8)).to(K.device)
     B.csm_compress_ex(K, V, N, L, n1, n2, c, r, head_mask=hm, seq_mask=sm, match_out=match,
-                      force_simt=force_simt, workspace=ws)
+                      kernel=kernel, workspace=ws)
     torch.cuda.synchronize()
     st = B.csmkv_device_status(ws)
     assert st == 0, f"device status {st}: {B.status_str(st)}"
     return match.cpu().numpy()
 
 
-def round_parity(K, V, N, L, n1, n2, c, r, dtype, head_mask=None, seq_mask=None, force_simt=0, max_dev_frac=0.01):
+def round_parity(K, V, N, L, n1, n2, c, r, dtype, head_mask=None, seq_mask=None, kernel=0, max_dev_frac=0.01):
     """Runs one device round in place and checks it against the oracle. Returns stats."""
     pre = snapshot(K, V, N, L)
     m = B.csm_edges_per_chunk(r, c)
-    gm = gpu_round(K, V, N, L, n1, n2, c, r, head_mask, seq_mask, force_simt)
+    gm = gpu_round(K, V, N, L, n1, n2, c, r, head_mask, seq_mask, kernel)
     post = snapshot(K, V, N, L)
     sk = skip_vector(K.shape[0], K.shape[1], head_mask, seq_mask)
     free = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk)
