@@ -39,6 +39,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 CSM_KERNELS = {"auto": 0, "simt": 1, "ring": 2, "split": 3}
+L2_BYTES = 128 << 20  # GB300 L2 is about 129 MB
 
 
 def peaks():
@@ -295,19 +296,29 @@ def run_gpu(args):
     csm_tokens_step = sum(t for t, _ in csm_stats)
     csm_bytes_step = sum(b_ for _, b_ in csm_stats)
 
-    ev_pool = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (len(rounds) + w.steps) + 8)]
-    marks = []
+    # per-call device timing: events recorded by the native loop around every call
+    n_pre = sum(1 for rd in rounds if rd.step == 0)
+    ev_pre = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pre)]
+    ev_att = [torch.cuda.Event(enable_timing=True) for _ in range(2 * w.steps)]
+    ev_csm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (len(rounds) - n_pre))]
+    for e in ev_pre + ev_att + ev_csm:  # torch creates events lazily, on first record
+        e.record(stream)
+    flush = None
+    if args.l2_flush == "on" or (args.l2_flush == "auto" and attn_bytes_step / w.steps < 2 * L2_BYTES):
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    pre_marks = []
 
     def hook(kind, what, before):
-        e = ev_pool[len(marks)]
+        e = ev_pre[len(pre_marks)]
         e.record(stream)
-        marks.append((kind, before, e))
+        pre_marks.append(e)
 
     def one_step(timed):
         for dst, src in ((d["K"], K0), (d["V"], V0), (d["N"], N0), (d["len"], L0)):
             dst.copy_(src, non_blocking=True)
-        marks.clear()
-        p.run(hook=hook if timed else None)
+        pre_marks.clear()
+        p.run_native(hook=hook if timed else None, attn_events=ev_att if timed else None,
+                     csm_events=ev_csm if timed else None, l2_flush=flush)
 
     for _ in range(args.warmup):
         one_step(False)
@@ -316,6 +327,7 @@ def run_gpu(args):
         torch.distributed.barrier()
     csm_ms = attn_ms = 0.0
     attn_calls = 0
+    round_ms = [0.0] * len(rounds)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
@@ -324,15 +336,14 @@ def run_gpu(args):
         for _ in range(args.steps):
             one_step(True)
             torch.cuda.synchronize()
-            for k in range(0, len(marks), 2):
-                kind, _, e0 = marks[k]
-                _, _, e1 = marks[k + 1]
-                dt = e0.elapsed_time(e1)
-                if kind == "csm":
-                    csm_ms += dt
-                else:
-                    attn_ms += dt
-                    attn_calls += 1
+            for k, e in enumerate(ev_pre[0::2] + ev_csm[0::2]):
+                e1 = (ev_pre[1::2] + ev_csm[1::2])[k]
+                dt = e.elapsed_time(e1)
+                round_ms[k] += dt / args.steps
+                csm_ms += dt
+            for k in range(0, len(ev_att), 2):
+                attn_ms += ev_att[k].elapsed_time(ev_att[k + 1])
+                attn_calls += 1
         t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -373,7 +384,9 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded AR(1) keys, N(0,1) values, N(0,I) queries; no model weights)",
-        "config": config_of(w),
+        "config": dict(config_of(w), l2=("a 2xL2 buffer is read before every attention call" if flush is not None
+                                          else "every attention call reads more than 2xL2 of cache"),
+                       csm_kernel=args.csm_kernel),
         "decode_attn": {"value": attn_gbs, "unit": "GB/s", "frac_of_measured_peak": attn_gbs / hbm,
                         "frac_of_nominal_7900": attn_gbs / 7900.0, "calls_timed": attn_calls,
                         "avg_call_us": 1e6 * avg_launch_s},
@@ -386,9 +399,13 @@ def run_gpu(args):
                          "csm_kernel": args.csm_kernel,
                          "peak_kind": kind, "bytes_per_step": csm_bytes_step},
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
-                "ms_per_step": csm_ms / args.steps, "rounds_per_step": len(rounds)},
+                "ms_per_step": csm_ms / args.steps, "rounds_per_step": len(rounds),
+                "rounds": [{"step": rd.step, "m": rd.m, "s_before": int(rd.s_before[0]), "ms": round_ms[k],
+                            "gbs": csm_stats[k][1] / (round_ms[k] / 1e3) / 1e9}
+                           for k, rd in enumerate(rounds)]},
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 * len(rounds) + (2 if w.batch * w.h_kv <= 2048 else 3) * w.steps),
+        "gpu_launches": args.steps * (2 * len(rounds) + ((2 if w.batch * w.h_kv <= 2048 else 3)
+                                                          + (1 if flush is not None else 0)) * w.steps),
         "clocks": clocks,
     }
     if cpu is not None:
@@ -445,16 +462,17 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     hk = d["k_dec"][:nsteps].cpu().pin_memory()
     hv = d["v_dec"][:nsteps].cpu().pin_memory()
     ho = torch.empty_like(p.out[:nsteps], device="cpu").pin_memory()
-    dq, dk, dv = torch.empty_like(d["q"][0]), torch.empty_like(d["k_dec"][0]), torch.empty_like(d["v_dec"][0])
+    dq, dk, dv = torch.empty_like(d["q"][:nsteps]), torch.empty_like(d["k_dec"][:nsteps]), torch.empty_like(
+        d["v_dec"][:nsteps])
+    dout = torch.empty_like(p.out[:nsteps])
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(nsteps):
-        dq.copy_(hq[i], non_blocking=True)
-        dk.copy_(hk[i], non_blocking=True)
-        dv.copy_(hv[i], non_blocking=True)
-        B.csm_append(d["K"], d["V"], d["N"], d["len"], dk, dv, None, p.ws_app)
-        B.decode_attn_logn(dq, d["K"], d["V"], d["N"], d["len"], p.out[i], p.ws_att)
-        ho[i].copy_(p.out[i], non_blocking=True)
+    dq.copy_(hq, non_blocking=True)
+    dk.copy_(hk, non_blocking=True)
+    dv.copy_(hv, non_blocking=True)
+    B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], dq, dk, dv, dout, w.n1, w.n2, w.c, rounds=(),
+                     head_mask=p.head_mask, ws_csm=p.ws_csm, ws_append=p.ws_app, ws_attn=p.ws_att, steps=nsteps)
+    ho.copy_(dout, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     lens = d["len"].cpu().numpy()
@@ -464,7 +482,7 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
             "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
             "compress, D2H compacted rows",
             "decode_attn_gbs_at_prefill_round_length": step_bytes * nsteps / att_s / 1e9,
-            "decode_step_h2d_bytes": int(dq.numel() * dq.element_size() * 1 + 2 * dk.numel() * dk.element_size()),
+            "decode_step_h2d_bytes": int((dq.numel() * dq.element_size() + 2 * dk.numel() * dk.element_size()) // nsteps),
             "decode_step_d2h_bytes": int(ho[0].numel() * ho[0].element_size())}
 
 
@@ -479,6 +497,8 @@ def main():
     ap.add_argument("--cpu-units", type=int, default=256,
                     help="(layer, KV head) units in the oracle's timed sample (about 10 s on 16 cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
+                    help="zero a 2xL2 buffer before every attention call (auto: when a call reads < 2xL2)")
     ap.add_argument("--csm-kernel", default="auto", choices=sorted(CSM_KERNELS),
                     help="compression kernel: auto, simt (CUDA cores), ring or split (tensor cores)")
     args = ap.parse_args()

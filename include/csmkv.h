@@ -196,7 +196,7 @@ int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t*
  * the workspace: the scratch is a fixed 16 MiB array inside the library, one
  * per GPU that loads it, held until the process exits.
  *  - Capacity: returns CSMKV_ERR_WORKSPACE when decode_attn_workspace_bytes(
- *    cache, h_q) exceeds 16 MiB (at head_dim 128 on 152 SMs: about 700
+ *    cache, h_q) exceeds 16 MiB (at head_dim 128 on 152 SMs: about 3700
  *    (sequence, KV head) units). Nothing is launched then.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
@@ -213,6 +213,80 @@ int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t*
 int decode_attn_logn_noalloc(const void* q, const void* K, const void* V, const int32_t* N,
                              const int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale,
                              void* out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The decode loop, issued natively   [Chelsea §三 算法流程, Algorithm 1
+ *                                     (decode phase); CentroidKV 技术摘要:
+ *                                     推理流水线]
+ *
+ * Runs decode steps i = first_step .. first_step + steps - 1 (1-based) of the
+ * serving loop back to back on one stream, each exactly as the separate calls
+ * would:
+ *     csm_append(k_new[i-1], v_new[i-1])           K=[K,k], V=[V,v], N=[N,1]
+ *     decode_attn_logn(q[i-1]) -> out[i-1]
+ *     csm_compress_ex(r) for every planned round with step == i, in order
+ * The trigger test s >= B + g and the ratio schedule stay with the caller
+ * (csm_should_trigger, csm_ratio): lengths after append and compression are
+ * known on the host without reading the device, so the caller lists the
+ * rounds up front. Issuing the loop from here keeps host time per step far
+ * below the GPU time of the step, which a per-call binding from an
+ * interpreter does not.
+ *
+ * q, out: device [steps_total][batch][h_q][head_dim]; k_new, v_new: device
+ *   [steps_total][batch][h_kv][head_dim], all in the cache dtype; step i uses
+ *   slice i-1.
+ * rounds: host array of n_rounds entries with step >= 1, sorted by step;
+ *   entries outside the steps run here are ignored. seq_mask as in
+ *   csm_compress (device, or NULL).
+ * Workspaces as for the separate calls, each zero-filled before first use.
+ * attn_events / csm_events: NULL, or host arrays of cudaEvent_t (2 per
+ *   attention call, 2 per round, in issue order; index 2k and 2k+1 for the
+ *   k-th call of this invocation), recorded on `stream` right before and
+ *   right after that call, for per-call device timing.
+ * l2_flush, l2_flush_bytes: NULL/0, or a device buffer (16-byte aligned, size
+ *   a multiple of 16) that is read in full before every attention call
+ *   (outside the attention events), so that each call reads the cache from HBM
+ *   rather than from the previous call's L2 residue; for cold-cache timing of
+ *   caches smaller than about twice L2. The buffer is only read, so L2 holds
+ *   no dirty lines afterwards.
+ * Returns the first error of any call (nothing after it is issued).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    int32_t step;            /* decode step after whose attention the round runs (>= 1) */
+    double r;                /* merge ratio of the round */
+    const uint8_t* seq_mask; /* device [batch], nonzero = compress; NULL = all */
+} csm_round_plan;
+
+typedef struct {
+    void* K;
+    void* V;
+    int32_t* N;
+    int32_t* len;
+    csmkv_cache cache;
+    int32_t h_q;
+    float scale;
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    void* out;
+    int32_t n1, n2, c;
+    const uint8_t* head_mask;
+    int32_t csm_kernel; /* csm_options.kernel for every round */
+    const csm_round_plan* rounds;
+    int32_t n_rounds;
+    void* ws_csm;
+    size_t ws_csm_bytes;
+    void* ws_append;
+    size_t ws_append_bytes;
+    void* ws_attn;
+    size_t ws_attn_bytes;
+    void* const* attn_events;
+    void* const* csm_events;
+    void* l2_flush;
+    size_t l2_flush_bytes;
+} csm_decode_loop;
+
+int csm_decode_run(const csm_decode_loop* loop, int32_t first_step, int32_t steps, void* stream);
 
 /* ------------------------------------------------------------------------
  * Host-side schedule helpers   [Chelsea §三 算法流程, Algorithm 1;

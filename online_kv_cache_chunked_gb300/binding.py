@@ -41,6 +41,24 @@ class CsmOptions(ctypes.Structure):
 CSM_KERNEL_AUTO, CSM_KERNEL_SIMT, CSM_KERNEL_TC_RING, CSM_KERNEL_TC_SPLIT = 0, 1, 2, 3
 
 
+class CsmRoundPlan(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int32), ("r", ctypes.c_double), ("seq_mask", ctypes.c_void_p)]
+
+
+class CsmDecodeLoop(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("N", ctypes.c_void_p), ("len", ctypes.c_void_p),
+                ("cache", Cache), ("h_q", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("n1", ctypes.c_int32), ("n2", ctypes.c_int32), ("c", ctypes.c_int32),
+                ("head_mask", ctypes.c_void_p), ("csm_kernel", ctypes.c_int32),
+                ("rounds", ctypes.POINTER(CsmRoundPlan)), ("n_rounds", ctypes.c_int32),
+                ("ws_csm", ctypes.c_void_p), ("ws_csm_bytes", ctypes.c_size_t),
+                ("ws_append", ctypes.c_void_p), ("ws_append_bytes", ctypes.c_size_t),
+                ("ws_attn", ctypes.c_void_p), ("ws_attn_bytes", ctypes.c_size_t),
+                ("attn_events", ctypes.POINTER(ctypes.c_void_p)), ("csm_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("l2_flush", ctypes.c_void_p), ("l2_flush_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 
 P = ctypes.c_void_p
@@ -61,6 +79,7 @@ _SIGS = {
     "decode_attn_workspace_bytes": (SZ, [CP, I32]),
     "decode_attn_logn": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
     "decode_attn_logn_noalloc": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P]),
+    "csm_decode_run": (ctypes.c_int, [ctypes.POINTER(CsmDecodeLoop), I32, I32, P]),
     "csm_budget": (F64, [I64, F64, I64]),
     "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
     "csm_ratio": (F64, [I32, F64, F64, F64]),
@@ -193,6 +212,45 @@ def decode_attn_logn_noalloc(q, K, V, N, length, out, scale=None, stream=None):
     rc = load().decode_attn_logn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache),
                                          h_q, float(scale), _ptr(out), _stream(stream))
     _check("decode_attn_logn_noalloc", rc)
+
+
+# ---------------------------------------------------------------- decode loop
+def _event_array(events):
+    if events is None:
+        return None
+    handles = []
+    for e in events:
+        h = e.cuda_event
+        if not h:
+            raise ValueError("events must have been recorded once (torch creates them lazily)")
+        handles.append(h)
+    return (ctypes.c_void_p * len(handles))(*handles)
+
+
+def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), head_mask=None,
+                   ws_csm=None, ws_append=None, ws_attn=None, first_step=1, steps=None, csm_kernel=0,
+                   attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None):
+    """Decode steps first_step .. first_step+steps-1 (1-based) issued natively: per step
+    append(k_new[i-1], v_new[i-1]), attention(q[i-1]) -> out[i-1], then the planned
+    rounds of that step. rounds: iterable of (step, r, seq_mask or None), sorted by step.
+    attn_events / csm_events: torch.cuda.Event lists (2 per call), recorded once before."""
+    cache = cache_desc(K)
+    if steps is None:
+        steps = q.shape[0] - first_step + 1
+    if scale is None:
+        scale = 1.0 / (K.shape[-1] ** 0.5)
+    rl = list(rounds)
+    rarr = (CsmRoundPlan * max(1, len(rl)))()
+    for k, (st, r, sm) in enumerate(rl):
+        rarr[k] = CsmRoundPlan(int(st), float(r), _ptr(sm))
+    ae, ce = _event_array(attn_events), _event_array(csm_events)
+    nb = lambda t: t.numel() * t.element_size() if t is not None else 0  # noqa: E731
+    loop = CsmDecodeLoop(_ptr(K), _ptr(V), _ptr(N), _ptr(length), cache, int(q.shape[2]), float(scale),
+                         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), int(n1), int(n2), int(c), _ptr(head_mask),
+                         int(csm_kernel), rarr, len(rl), _ptr(ws_csm), nb(ws_csm), _ptr(ws_append), nb(ws_append),
+                         _ptr(ws_attn), nb(ws_attn), ae, ce, _ptr(l2_flush), nb(l2_flush))
+    rc = load().csm_decode_run(ctypes.byref(loop), int(first_step), int(steps), _stream(stream))
+    _check("csm_decode_run", rc)
 
 
 # ---------------------------------------------------------------- host helpers

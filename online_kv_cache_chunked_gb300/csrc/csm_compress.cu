@@ -291,14 +291,10 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     const int smem = csm_stage_bytes_simt(c, RB) + (int)sizeof(CsmTables) + 257 * 4 + 1024;
     if (smem > 227 * 1024) return CSMKV_ERR_UNSUPPORTED;
     if (cache->dtype == CSMKV_BF16) {
-        if (cudaFuncSetAttribute(csm_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return CSMKV_ERR_CUDA;
+        if (set_kernel_smem((const void*)csm_simt_kernel<__nv_bfloat16>, smem) != CSMKV_OK) return CSMKV_ERR_CUDA;
         csm_simt_kernel<__nv_bfloat16><<<sm_count(), kCsmThreads, smem, st>>>(P);
     } else {
-        if (cudaFuncSetAttribute(csm_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return CSMKV_ERR_CUDA;
+        if (set_kernel_smem((const void*)csm_simt_kernel<float>, smem) != CSMKV_OK) return CSMKV_ERR_CUDA;
         csm_simt_kernel<float><<<sm_count(), kCsmThreads, smem, st>>>(P);
     }
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;

@@ -504,13 +504,11 @@ int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint6
     if (grid <= 0) return CSMKV_ERR_CUDA;
     if (D == 128) {
         auto kern = csm_tc_kernel<128>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<128>::kSmem) != cudaSuccess)
-            return CSMKV_ERR_CUDA;
+        if (set_kernel_smem((const void*)kern, TcRing<128>::kSmem) != CSMKV_OK) return CSMKV_ERR_CUDA;
         kern<<<grid, kTcThreads, TcRing<128>::kSmem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
     } else {
         auto kern = csm_tc_kernel<64>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcRing<64>::kSmem) != cudaSuccess)
-            return CSMKV_ERR_CUDA;
+        if (set_kernel_smem((const void*)kern, TcRing<64>::kSmem) != CSMKV_OK) return CSMKV_ERR_CUDA;
         kern<<<grid, kTcThreads, TcRing<64>::kSmem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
     }
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;

@@ -364,9 +364,7 @@ int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint
     const int grid = 3 * sm_count();
     if (grid <= 0) return CSMKV_ERR_CUDA;
     auto run = [&](auto kern, int smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-            return (int)CSMKV_ERR_CUDA;
+        if (set_kernel_smem((const void*)kern, smem, true) != CSMKV_OK) return (int)CSMKV_ERR_CUDA;
         kern<<<grid, kTc3Threads, smem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
         return cudaGetLastError() == cudaSuccess ? (int)CSMKV_OK : (int)CSMKV_ERR_CUDA;
     };

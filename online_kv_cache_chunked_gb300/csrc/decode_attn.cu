@@ -12,8 +12,9 @@
 // columns) and the degree tile into a 3-stage TMA/mbarrier ring; four consumer
 // warps each take 16 tokens of a tile and run S^T = K q^T and O^T += V^T P^T on
 // mma.sync (bf16 in, fp32 accumulate), the G <= 8 query heads of the group in
-// the N = 8 dimension, so each K/V byte is read once for the whole group. Each
-// warp writes one partial (m, l, acc) per unit it touched; the last CTA to
+// the N = 8 dimension, so each K/V byte is read once for the whole group. The
+// CTA merges its warps' states in shared memory and writes one partial
+// (m, l, acc) per unit it touched; the last CTA to
 // finish its part of a unit (a per-unit counter) merges the unit's partials into
 // the output. Unit offsets come from a block-wide scan of the lengths inside
 // every CTA (or, for batches of more than 2048 units, from a one-CTA prologue).
@@ -145,8 +146,20 @@ struct RangeWalker {
     }
 };
 
+// Shared scratch for merging partial softmax states: per-warp head maxima and
+// sums, and one fp32 row per head. The head stride of 132 floats puts the
+// fragment stores of a warp (lanes 4g + t4 -> head 2 t4 or 2 t4 + 1, dim g) on
+// 32 distinct banks.
+constexpr int kRedStride = 132;
+struct CombineScratch {
+    float m[kConsumerWarps][kSlotHeads];
+    float l[kConsumerWarps][kSlotHeads];
+    float acc[kSlotHeads][kRedStride];
+};
+
 // Scratch of the main kernel after the stage ring.
 struct DecSmall {
+    CombineScratch cs;
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int abort_flag;
@@ -160,49 +173,106 @@ __device__ __forceinline__ void consumer_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Merges the partials of `unit` (written by CTAs c0..c1, 4 warps each) into the
-// output; run by the 4 consumer warps of the last contributing CTA.
+// Merges the partials of `unit` -- one record per contributing CTA c0..c1, a
+// contiguous run -- into the output; run by the 4 consumer warps of the last
+// contributing CTA, so it sits on the kernel's tail: records are spread over
+// all 128 threads with several loads in flight per thread, and the cross-warp
+// sums go through shared memory in warp order (deterministic).
 template <int D>
-__device__ void combine_unit(const DecParams& p, int unit, int c0, int c1, int warp, int lane) {
-    constexpr int PER = D / 32;  // output dims per lane
-    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
-    for (int g = warp; g < p.G; g += kConsumerWarps) {
-        float M = -INFINITY;
-        for (int c = c0; c <= c1; ++c)
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M = fmaxf(M, __ldcg(p.pm + (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + g));
-        float acc[PER], L = 0.f;
+__device__ void combine_unit(const DecParams& p, int unit, int c0, int c1, int warp, int lane, CombineScratch& cs) {
+    constexpr int PER = D / 32;  // dims per lane
+    const int tid = warp * 32 + lane;
+    const int G = p.G;
+    const int nrec = c1 - c0 + 1;
+    const size_t rec0 = (size_t)c0 + unit;
+
+    // pass 1: per-head maximum over the records
+    float mx[kSlotHeads];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-        for (int c = c0; c <= c1; ++c)
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const size_t rec = (((size_t)c + unit) * kConsumerWarps + w) * kSlotHeads + g;
-                const float mw = __ldcg(p.pm + rec);
-                if (mw == -INFINITY) continue;  // that warp saw no token of the unit
-                const float f = exp2f(mw - M);
-                L = fmaf(f, __ldcg(p.pl + rec), L);
-                const float* a = p.pacc + rec * D + lane * PER;
+    for (int g = 0; g < kSlotHeads; ++g) mx[g] = -INFINITY;
+    for (int r = tid; r < nrec; r += kConsumerWarps * 32) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.pm + (rec0 + r) * kSlotHeads));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(p.pm + (rec0 + r) * kSlotHeads + 4));
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int g = 0; g < kSlotHeads; ++g)
+            if (g < G) mx[g] = fmaxf(mx[g], v[g]);
+    }
+#pragma unroll
+    for (int g = 0; g < kSlotHeads; ++g) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < kSlotHeads; ++g) cs.m[warp][g] = mx[g];
+    }
+    consumer_barrier();
+    float M[kSlotHeads];
+#pragma unroll
+    for (int g = 0; g < kSlotHeads; ++g) M[g] = fmaxf(fmaxf(cs.m[0][g], cs.m[1][g]), fmaxf(cs.m[2][g], cs.m[3][g]));
+
+    // pass 2: warp w folds records w, w+4, ...; lane covers PER dims of every head
+    float acc[kSlotHeads][PER], L[kSlotHeads];
+#pragma unroll
+    for (int g = 0; g < kSlotHeads; ++g) {
+        L[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[g][i] = 0.f;
+    }
+#pragma unroll 4
+    for (int r = warp; r < nrec; r += kConsumerWarps) {
+        const size_t rec = rec0 + r;
+        const float4 ma = __ldcg(reinterpret_cast<const float4*>(p.pm + rec * kSlotHeads));
+        const float4 mb = __ldcg(reinterpret_cast<const float4*>(p.pm + rec * kSlotHeads + 4));
+        const float4 la = __ldcg(reinterpret_cast<const float4*>(p.pl + rec * kSlotHeads));
+        const float4 lb = __ldcg(reinterpret_cast<const float4*>(p.pl + rec * kSlotHeads + 4));
+        const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+        for (int g = 0; g < kSlotHeads; ++g) {
+            if (g < G) {
+                // a CTA that saw no token of a head left m = -inf, l = 0, acc = 0
+                const float f = mv[g] == -INFINITY ? 0.f : exp2f(mv[g] - M[g]);
+                L[g] = fmaf(f, lv[g], L[g]);
+                const float* a = p.pacc + (rec * kSlotHeads + g) * D + lane * PER;
                 if constexpr (PER == 4) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(a));
-                    acc[0] = fmaf(f, v.x, acc[0]);
-                    acc[1] = fmaf(f, v.y, acc[1]);
-                    acc[2] = fmaf(f, v.z, acc[2]);
-                    acc[3] = fmaf(f, v.w, acc[3]);
+                    acc[g][0] = fmaf(f, v.x, acc[g][0]);
+                    acc[g][1] = fmaf(f, v.y, acc[g][1]);
+                    acc[g][2] = fmaf(f, v.z, acc[g][2]);
+                    acc[g][3] = fmaf(f, v.w, acc[g][3]);
                 } else {
                     const float2 v = __ldcg(reinterpret_cast<const float2*>(a));
-                    acc[0] = fmaf(f, v.x, acc[0]);
-                    acc[1] = fmaf(f, v.y, acc[1]);
+                    acc[g][0] = fmaf(f, v.x, acc[g][0]);
+                    acc[g][1] = fmaf(f, v.y, acc[g][1]);
                 }
             }
-        const float inv = 1.0f / L;
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D +
-                           lane * PER;
-        if constexpr (PER == 4) {
-            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                      pack_bf16x2(acc[2] * inv, acc[3] * inv));
-        } else {
-            *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
         }
+    }
+
+    // cross-warp sums in warp order
+    for (int w = 0; w < kConsumerWarps; ++w) {
+        if (warp == w) {
+#pragma unroll
+            for (int g = 0; g < kSlotHeads; ++g) {
+                if (g < G) {
+                    float* row = &cs.acc[g][lane * PER];
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) row[i] = (w == 0) ? acc[g][i] : row[i] + acc[g][i];
+                    if (lane == 0) cs.l[w][g] = L[g];
+                }
+            }
+        }
+        consumer_barrier();
+    }
+    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
+    for (int i = tid; i < G * (D / 4); i += kConsumerWarps * 32) {
+        const int g = i / (D / 4), d = (i - g * (D / 4)) * 4;
+        const float inv = 1.0f / ((cs.l[0][g] + cs.l[1][g]) + (cs.l[2][g] + cs.l[3][g]));
+        const float4 v = *reinterpret_cast<const float4*>(&cs.acc[g][d]);
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * G + g) * D + d;
+        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(v.x * inv, v.y * inv), pack_bf16x2(v.z * inv, v.w * inv));
     }
 }
 
@@ -479,25 +549,63 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             ok = false;
             break;
         }
-        // ---- partial of (this CTA, this unit, this warp)
+        // ---- one partial per (CTA, unit): the 4 warps' states merged in shared memory,
+        //      in warp order (deterministic), then written as one record
         float lt0 = l0, lt1 = l1;
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
             lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
         }
-        const size_t slot = ((size_t)blockIdx.x + unit) * kConsumerWarps + warp;
+        CombineScratch& cs = sm.cs;
         const int h0 = 2 * t4, h1 = 2 * t4 + 1;
         if (g == 0) {
-            if (h0 < p.G) { p.pm[slot * kSlotHeads + h0] = m0; p.pl[slot * kSlotHeads + h0] = lt0; }
-            if (h1 < p.G) { p.pm[slot * kSlotHeads + h1] = m1; p.pl[slot * kSlotHeads + h1] = lt1; }
+            cs.m[warp][h0] = m0;
+            cs.m[warp][h1] = m1;
+            cs.l[warp][h0] = lt0;
+            cs.l[warp][h1] = lt1;
         }
-        float* acc0 = p.pacc + (slot * kSlotHeads + h0) * D;
-        float* acc1 = p.pacc + (slot * kSlotHeads + h1) * D;
+        consumer_barrier();
+        {
+            const float M0 = fmaxf(fmaxf(cs.m[0][h0], cs.m[1][h0]), fmaxf(cs.m[2][h0], cs.m[3][h0]));
+            const float M1 = fmaxf(fmaxf(cs.m[0][h1], cs.m[1][h1]), fmaxf(cs.m[2][h1], cs.m[3][h1]));
+            const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+            const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                if (warp == w) {
 #pragma unroll
-        for (int mb = 0; mb < D / 16; ++mb) {
-            if (h0 < p.G) { acc0[16 * mb + g] = oacc[mb][0]; acc0[16 * mb + g + 8] = oacc[mb][2]; }
-            if (h1 < p.G) { acc1[16 * mb + g] = oacc[mb][1]; acc1[16 * mb + g + 8] = oacc[mb][3]; }
+                    for (int mb = 0; mb < D / 16; ++mb) {
+                        float* r0 = &cs.acc[h0][16 * mb + g];
+                        float* r1 = &cs.acc[h1][16 * mb + g];
+                        if (w == 0) {
+                            r0[0] = f0 * oacc[mb][0];
+                            r1[0] = f1 * oacc[mb][1];
+                            r0[8] = f0 * oacc[mb][2];
+                            r1[8] = f1 * oacc[mb][3];
+                        } else {
+                            r0[0] = fmaf(f0, oacc[mb][0], r0[0]);
+                            r1[0] = fmaf(f1, oacc[mb][1], r1[0]);
+                            r0[8] = fmaf(f0, oacc[mb][2], r0[8]);
+                            r1[8] = fmaf(f1, oacc[mb][3], r1[8]);
+                        }
+                    }
+                }
+                consumer_barrier();
+            }
+        }
+        const size_t slot = (size_t)blockIdx.x + unit;
+        for (int i = tid; i < p.G * (D / 4); i += kConsumerWarps * 32) {
+            const int h = i / (D / 4), d = (i - h * (D / 4)) * 4;
+            __stcg(reinterpret_cast<float4*>(p.pacc + (slot * kSlotHeads + h) * D + d),
+                   *reinterpret_cast<const float4*>(&cs.acc[h][d]));
+        }
+        if (tid < p.G) {
+            const float M = fmaxf(fmaxf(cs.m[0][tid], cs.m[1][tid]), fmaxf(cs.m[2][tid], cs.m[3][tid]));
+            float L = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w)
+                if (cs.m[w][tid] != -INFINITY) L = fmaf(exp2f(cs.m[w][tid] - M), cs.l[w][tid], L);
+            p.pm[slot * kSlotHeads + tid] = M;
+            p.pl[slot * kSlotHeads + tid] = L;
         }
         // ---- the last CTA to finish its part of the unit merges every part
         __threadfence();
@@ -512,7 +620,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         consumer_barrier();
         if (sm.last) {
             __threadfence();
-            combine_unit<D>(p, unit, c0, c1, warp, lane);
+            combine_unit<D>(p, unit, c0, c1, warp, lane, sm.cs);
         }
         consumer_barrier();  // sm.last is rewritten for the next unit
     }
@@ -587,7 +695,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const DecParams p, cons
 static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, size_t* o_cta, size_t* o_cnt,
                          size_t* o_pm, size_t* o_pl, size_t* o_pacc) {
     const size_t BH = (size_t)cache->batch * cache->h_kv;
-    const size_t slots = ((size_t)nCTA + BH) * kConsumerWarps;
+    const size_t slots = (size_t)nCTA + BH;  // one record per (CTA, unit it touches)
     size_t off = kHeaderBytes;
     *o_prefix = off;
     off = align_up(off + (BH + 1) * 4, 256);
@@ -609,9 +717,9 @@ static int launch_decode_bf16(const DecParams& P, const CUtensorMap& tk, const C
                               const CUtensorMap& tn, cudaStream_t st) {
     constexpr int smem = kStages * DecGeom<D>::kStageBytes + (int)sizeof(DecSmall) +
                          (SCAN ? (kMaxScanUnits + 1) * 4 : 0) + 1024;
+    static_assert(kDecCtasPerSm * (smem + 1024) <= 228 * 1024, "two CTAs per SM must fit in shared memory");
     auto kern = decode_main_kernel<D, SCAN>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return CSMKV_ERR_CUDA;
+    if (set_kernel_smem((const void*)kern, smem) != CSMKV_OK) return CSMKV_ERR_CUDA;
     kern<<<P.nCTA, kDecThreads, smem, st>>>(P, tk, tv, tn);
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
 }

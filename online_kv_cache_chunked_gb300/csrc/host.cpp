@@ -20,6 +20,36 @@ int sm_count() {
     return cache[dev];
 }
 
+namespace {
+struct SmemSetting {
+    int dev;
+    const void* fn;
+    int bytes;
+};
+std::mutex g_smem_mu;
+SmemSetting g_smem[256];
+int g_smem_n = 0;
+}  // namespace
+
+int set_kernel_smem(const void* fn, int bytes, bool max_carveout) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSMKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    int k = 0;
+    while (k < g_smem_n && !(g_smem[k].dev == dev && g_smem[k].fn == fn)) ++k;
+    if (k < g_smem_n && g_smem[k].bytes >= bytes) return CSMKV_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return CSMKV_ERR_CUDA;
+    if (max_carveout && cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return CSMKV_ERR_CUDA;
+    if (k < g_smem_n) {
+        g_smem[k].bytes = bytes;
+    } else if (g_smem_n < 256) {  // a full table only means the attribute is set again on later calls
+        g_smem[g_smem_n++] = SmemSetting{dev, fn, bytes};
+    }
+    return CSMKV_OK;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

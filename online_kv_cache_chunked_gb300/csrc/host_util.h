@@ -45,6 +45,10 @@ inline int check_cache(const csmkv_cache* c) {
 }
 
 int sm_count();                 // SMs of the current device (cached per device)
+// Raises a kernel's dynamic shared-memory limit on the current device (and, if
+// asked, prefers the largest shared-memory carveout). The setting is remembered
+// per (device, kernel), so repeated launches cost no runtime call.
+int set_kernel_smem(const void* fn, int bytes, bool max_carveout = false);
 const void* encode_fn();        // cuTensorMapEncodeTiled, or nullptr
 
 // Encodes a tiled tensor map; returns false on failure.

@@ -152,6 +152,22 @@ class Pipeline:
         self.compress_at(i, hook)
 
     def run(self, hook=None, steps=None):
+        """Prefill round(s), then the decode loop one binding call per kernel."""
         self.compress_at(0, hook)
         for i in range(1, (self.w.steps if steps is None else steps) + 1):
             self.decode_step(i, hook)
+
+    def decode_plan(self):
+        """(step, r, seq_mask) of every round after prefill, in issue order."""
+        return [(rd.step, rd.r, self.masks[k]) for k, rd in enumerate(self.rounds) if rd.step >= 1]
+
+    def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None):
+        """Prefill round(s), then the whole decode loop issued by the library in one call."""
+        d, w = self.d, self.w
+        self.compress_at(0, hook)
+        n = w.steps if steps is None else steps
+        B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], d["q"], d["k_dec"], d["v_dec"], self.out, w.n1, w.n2,
+                         w.c, rounds=self.decode_plan(), head_mask=self.head_mask, ws_csm=self.ws_csm,
+                         ws_append=self.ws_app, ws_attn=self.ws_att, first_step=1, steps=n,
+                         csm_kernel=self.csm_kernel, attn_events=attn_events, csm_events=csm_events,
+                         l2_flush=l2_flush, stream=self.stream)

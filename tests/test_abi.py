@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted([
         "csm_workspace_bytes", "csm_compress", "csm_compress_ex", "csm_max_chunks", "csm_append_workspace_bytes",
         "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "decode_attn_logn_noalloc",
-        "csm_budget", "csm_should_trigger",
+        "csm_decode_run", "csm_budget", "csm_should_trigger",
         "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
         "csmkv_clear_status", "csmkv_status_str"]), names
     raw = ctypes.CDLL(_build.OUT)
@@ -129,3 +129,24 @@ def test_attention_argument_errors_without_gpu(lib):
     assert call(h_q=18) == 8         # bf16 group of 9 query heads is not covered
     assert call(cache=_cache(head_dim=96)) == 8
     assert lib.csm_append(None, None, None, None, ctypes.byref(c), None, None, None, None, 0, None) == 1
+
+
+def test_decode_run_rejects_bad_arguments_without_a_gpu(lib):
+    fn = lib.csm_decode_run
+    assert fn(None, 1, 1, None) == 1  # CSMKV_ERR_ARG: no loop description
+    loop = B.CsmDecodeLoop()
+    assert fn(ctypes.byref(loop), 0, 1, None) == 1  # steps are 1-based
+    assert fn(ctypes.byref(loop), 1, -1, None) == 1
+    assert fn(ctypes.byref(loop), 1, 0, None) == 0  # nothing to do
+    assert fn(ctypes.byref(loop), 1, 3, None) == 1  # no inputs
+    rounds = (B.CsmRoundPlan * 2)(B.CsmRoundPlan(5, 0.5, None), B.CsmRoundPlan(2, 0.5, None))
+    x = ctypes.c_void_p(16)
+    loop = B.CsmDecodeLoop(q=x, k_new=x, v_new=x, out=x, rounds=rounds, n_rounds=2)
+    assert fn(ctypes.byref(loop), 1, 3, None) == 1  # rounds out of step order
+    rounds[1].step = 7
+    assert fn(ctypes.byref(loop), 1, 3, None) == 1  # the zeroed cache descriptor (batch 0)
+    loop.cache = B.Cache(1, 2, 128, 1024, 7)
+    assert fn(ctypes.byref(loop), 1, 3, None) == 2  # unknown dtype
+    loop.cache = B.Cache(1, 2, 128, 1024, 0)
+    loop.l2_flush = x
+    assert fn(ctypes.byref(loop), 1, 3, None) == 1  # a flush buffer without a size

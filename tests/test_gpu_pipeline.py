@@ -62,3 +62,32 @@ def test_ragged_batch_pipeline_lengths(cuda_lib):
     b = 5
     attn_parity(d["q"][-1][b:b + 1], d["K"][b:b + 1], d["V"][b:b + 1], d["N"][b:b + 1], d["len"][b:b + 1],
                 p.out[-1][b:b + 1], "bf16")
+
+
+@pytest.mark.parametrize("name,steps", [("llama_32k_b4", 12), ("qwen2_ragged", 40)])
+def test_native_loop_matches_per_call_loop(cuda_lib, name, steps):
+    """The library-issued decode loop gives bit-identical caches and outputs to the
+    same calls made one by one through the binding (rounds at decode steps included)."""
+    from online_kv_cache_chunked_gb300 import binding as B
+    w = synth.scaled(synth.WORKLOADS[name], steps=steps)
+    d1 = synth.make_device(w)
+    d2 = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d1.items()}
+    p1, p2 = Pipeline(w, d1), Pipeline(w, d2)
+    assert any(rd.step >= 1 for rd in p1.rounds)
+    p1.run()
+    stream = torch.cuda.current_stream()
+    ev_att = [torch.cuda.Event(enable_timing=True) for _ in range(2 * w.steps)]
+    ev_csm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(p2.decode_plan()))]
+    for e in ev_att + ev_csm:
+        e.record(stream)
+    flush = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    p2.run_native(attn_events=ev_att, csm_events=ev_csm, l2_flush=flush)
+    torch.cuda.synchronize()
+    for ws in (p2.ws_csm, p2.ws_app, p2.ws_att):
+        assert B.csmkv_device_status(ws) == 0
+    for k in ("K", "V", "N", "len"):
+        assert torch.equal(d1[k], d2[k]), k
+    assert torch.equal(p1.out, p2.out)
+    assert np.array_equal(d2["len"].cpu().numpy(), final_lengths(w))
+    assert all(ev_att[2 * i].elapsed_time(ev_att[2 * i + 1]) > 0 for i in range(w.steps))
+    assert all(ev_csm[2 * i].elapsed_time(ev_csm[2 * i + 1]) > 0 for i in range(len(ev_csm) // 2))

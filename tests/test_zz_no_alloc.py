@@ -43,8 +43,9 @@ def test_no_workspace_matches_workspace_entry_point_twice(cuda_lib):
 
 
 def test_no_workspace_rejects_batches_beyond_its_scratch(cuda_lib):
-    # 4096 units need far more than the fixed 16 MiB scratch: refused before any launch
-    cache = B.Cache(512, 8, 128, 1024, B.BF16)
+    # 16384 units need far more than the fixed 16 MiB scratch: refused before any launch
+    assert B.decode_attn_workspace_bytes(B.Cache(2048, 8, 128, 1024, B.BF16), 32) > (16 << 20)
+    cache = B.Cache(2048, 8, 128, 1024, B.BF16)
     P = ctypes.c_void_p
     rc = B.load().decode_attn_logn_noalloc(P(4096), P(4096), P(4096), P(4096), P(4096), ctypes.byref(cache), 32,
                                            0.088, P(4096), None)
