@@ -169,6 +169,12 @@ struct DecSmall {
     int warp_tot[kDecThreads / 32];
 };
 
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void consumer_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
@@ -607,21 +613,19 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             p.pm[slot * kSlotHeads + tid] = M;
             p.pl[slot * kSlotHeads + tid] = L;
         }
-        // ---- the last CTA to finish its part of the unit merges every part
-        __threadfence();
+        // ---- the last CTA to finish its part of the unit merges every part. One
+        //      acq_rel atomic both publishes this CTA's record (its stores are ordered
+        //      before it by the barrier) and, for the last CTA, acquires the others'.
         consumer_barrier();
         const int c0 = pre[unit] / W, c1 = (pre[unit + 1] - 1) / W;
         if (tid == 0) {
-            const int prev = atomicAdd(p.counter + unit, 1);
+            const int prev = atom_add_acq_rel_gpu(p.counter + unit, 1);
             const int last = prev == c1 - c0;
             if (last) p.counter[unit] = 0;  // ready for the next call
             sm.last = last;
         }
         consumer_barrier();
-        if (sm.last) {
-            __threadfence();
-            combine_unit<D>(p, unit, c0, c1, warp, lane, sm.cs);
-        }
+        if (sm.last) combine_unit<D>(p, unit, c0, c1, warp, lane, sm.cs);
         consumer_barrier();  // sm.last is rewritten for the next unit
     }
     if (!ok && tid == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
