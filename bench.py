@@ -76,20 +76,26 @@ def attn_bytes(w, lengths_units):
     return int(lengths_units.sum()) * row_bytes(w) + w.batch * w.h_q * w.d * e * 2
 
 
-def source_sha(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "online_kv_cache_chunked_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_file):
-    """ncu DRAM bytes per launch for a kernel, if taken on the current source."""
+def traffic_record(kernel, key):
+    """ncu DRAM bytes (per launch or per step) of a kernel, if taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p)).get(os.path.basename(kernel_file))
+    rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, "online_kv_cache_chunked_gb300", "csrc", os.path.basename(kernel_file))
-    return rec.get("bytes_per_launch") if rec.get("source_sha") == source_sha(src) else None
+    try:
+        ok = rec.get("source_sha") == source_sha(rec.get("files", []))
+    except OSError:
+        ok = False
+    return rec.get(key) if ok else None
 
 
 class Clocks:
@@ -392,10 +398,10 @@ def run_gpu(args):
                         "avg_call_us": 1e6 * avg_launch_s},
         "roofline": {"bound": "hbm", "achieved": per_launch_bytes / avg_launch_s / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": per_launch_bytes / avg_launch_s / 1e9 / hbm,
-                     "traffic": traffic_record("decode_attn.cu"), "kernel": "decode_attn_logn",
+                     "traffic": traffic_record("decode_attn", "bytes_per_launch"), "kernel": "decode_attn_logn",
                      "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
         "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
-                         "traffic": traffic_record("csm_compress.cu"), "kernel": "csm_compress",
+                         "traffic": traffic_record("csm_compress", "bytes_per_step"), "kernel": "csm_compress",
                          "csm_kernel": args.csm_kernel,
                          "peak_kind": kind, "bytes_per_step": csm_bytes_step},
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
