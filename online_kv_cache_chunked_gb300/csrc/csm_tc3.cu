@@ -109,34 +109,56 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
     };
     // m == H: every merged B row replaces its own shared-memory row (same arithmetic
     // as emit_rows: fp32 sums in A order, scaled by 1 / degree sum, rounded once).
+    // Four threads per 64-column box of a row, two 16-byte pieces each, so the
+    // per-row work (row lookup, member scan, swizzle terms) is paid once per 32
+    // bytes; threads of the second box take their two pieces in the other order,
+    // so a quarter warp (one row) reads 8 distinct bank groups at every step.
     auto merge_inplace = [&](const int32_t* sN) {
-        constexpr int PR = D / 8;
-        const int n = sm.nmerged * PR;
+        constexpr int TPR = 4 * R::kBoxes;  // threads per row; divides the block size
+        const int sub = tid % TPR;
+        const int box = sub >> 2;
+        const uint32_t c0 = (uint32_t)((sub & 3) * 2 + (box & 1)), c1 = c0 ^ 1u;
+        uint8_t* const abox = slot + box * 16384;
+        uint8_t* const bbox = slot + (R::kBoxes + box) * 16384;
+        const int n = sm.nmerged * TPR;
         for (int i = tid; i < n; i += kTc3Threads) {
-            const int k = i / PR, cc = i - k * PR;
-            const int b = sm.mlist[k], q = 2 * b + 1;
-            uint4* dst = reinterpret_cast<uint4*>(piece(q, cc));
-            float acc[8], f[8];
-            Elem<T>::unpack(*dst, f);
-            const float nb = (float)sN[q];
+            const int b = sm.mlist[i / TPR];
+            const uint32_t xb = (uint32_t)(b & 7);
+            uint4* const d0 = reinterpret_cast<uint4*>(bbox + b * 128 + ((c0 ^ xb) << 4));
+            uint4* const d1 = reinterpret_cast<uint4*>(bbox + b * 128 + ((c1 ^ xb) << 4));
+            float acc0[8], acc1[8], f[8];
+            const float nb = (float)sN[2 * b + 1];
+            Elem<T>::unpack(*d0, f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = nb * f[e];
+            for (int e = 0; e < 8; ++e) acc0[e] = nb * f[e];
+            Elem<T>::unpack(*d1, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc1[e] = nb * f[e];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 uint32_t bits = sm.mask[b][w];
                 while (bits) {
-                    const int qa = 2 * (w * 32 + __ffs(bits) - 1);
+                    const int a = w * 32 + __ffs(bits) - 1;
                     bits &= bits - 1u;
-                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(piece(qa, cc)), f);
-                    const float na = (float)sN[qa];
+                    const uint8_t* const arow = abox + a * 128;
+                    const uint32_t xa = (uint32_t)(a & 7);
+                    const float na = (float)sN[2 * a];
+                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(arow + ((c0 ^ xa) << 4)), f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(na, f[e], acc[e]);
+                    for (int e = 0; e < 8; ++e) acc0[e] = fmaf(na, f[e], acc0[e]);
+                    Elem<T>::unpack(*reinterpret_cast<const uint4*>(arow + ((c1 ^ xa) << 4)), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc1[e] = fmaf(na, f[e], acc1[e]);
                 }
             }
             const float inv = sm.ninv[b];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= inv;
-            *dst = Elem<T>::pack(acc);
+            for (int e = 0; e < 8; ++e) {
+                acc0[e] *= inv;
+                acc1[e] *= inv;
+            }
+            *d0 = Elem<T>::pack(acc0);
+            *d1 = Elem<T>::pack(acc1);
         }
     };
     auto store_b_rows = [&](const CUtensorMap* map, long long row) {  // thread 0
