@@ -250,6 +250,10 @@ int decode_attn_logn_noalloc(const void* q, const void* K, const void* V, const 
  *   caches smaller than about twice L2. The buffer is only read, so L2 holds
  *   no dirty lines afterwards.
  * Returns the first error of any call (nothing after it is issued).
+ * Everything is enqueued on `stream` without host synchronisation, so a call
+ * with attn_events, csm_events and l2_flush all NULL can be captured into a
+ * CUDA graph (after one direct call has set the kernels' attributes) and the
+ * graph replayed on the same buffers.
  * ---------------------------------------------------------------------- */
 typedef struct {
     int32_t step;            /* decode step after whose attention the round runs (>= 1) */

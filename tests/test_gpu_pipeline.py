@@ -91,3 +91,31 @@ def test_native_loop_matches_per_call_loop(cuda_lib, name, steps):
     assert np.array_equal(d2["len"].cpu().numpy(), final_lengths(w))
     assert all(ev_att[2 * i].elapsed_time(ev_att[2 * i + 1]) > 0 for i in range(w.steps))
     assert all(ev_csm[2 * i].elapsed_time(ev_csm[2 * i + 1]) > 0 for i in range(len(ev_csm) // 2))
+
+
+def test_decode_loop_replays_from_a_cuda_graph(cuda_lib):
+    """The library-issued decode loop (appends, attention, the rounds fired at steps 1
+    and 2) only enqueues device work, so it can be captured into one CUDA graph; a
+    replay gives the same caches and outputs, bit for bit, as the loop run directly."""
+    from online_kv_cache_chunked_gb300 import binding as B
+    w = synth.scaled(synth.WORKLOADS["llama_32k_b4"], steps=8)
+    d1 = synth.make_device(w)
+    d2 = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d1.items()}
+    p1, p2 = Pipeline(w, d1), Pipeline(w, d2)
+    assert [rd.step for rd in p1.rounds] == [0, 1, 2]
+    p1.run_native()
+    p2.compress_at(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.csm_decode_run(d2["K"], d2["V"], d2["N"], d2["len"], d2["q"], d2["k_dec"], d2["v_dec"], p2.out, w.n1,
+                         w.n2, w.c, rounds=p2.decode_plan(), head_mask=p2.head_mask, ws_csm=p2.ws_csm,
+                         ws_append=p2.ws_app, ws_attn=p2.ws_att, steps=w.steps)
+    g.replay()
+    torch.cuda.synchronize()
+    for ws in (p2.ws_csm, p2.ws_app, p2.ws_att):
+        assert B.csmkv_device_status(ws) == 0
+    for k in ("K", "V", "N", "len"):
+        assert torch.equal(d1[k], d2[k]), k
+    assert torch.equal(p1.out, p2.out)
+    assert np.array_equal(d2["len"].cpu().numpy(), final_lengths(w))
