@@ -26,6 +26,7 @@ import hashlib
 import json
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -108,7 +109,8 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples go to a temporary file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"csmkv_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
