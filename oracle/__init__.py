@@ -57,7 +57,7 @@ def _load():
         lib.oracle_csm_chunk.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_csm_chunk.restype = ctypes.c_int
         lib.oracle_csm_round.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
-                                         P, P, P, P, P, P, i32, P, P, i32]
+                                         P, P, P, P, P, P, i32, P, P, P, i32]
         lib.oracle_csm_round.restype = ctypes.c_int
         lib.oracle_csm_chunks.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, i32]
         lib.oracle_csm_chunks.restype = ctypes.c_int
@@ -128,13 +128,15 @@ def csm_chunks(Kc, Vc, Nc, m: int, forced=None, nthreads=None):
 
 
 def csm_round(K, V, N, length, n1: int, n2: int, c: int, m: int, skip=None,
-              forced=None, nthreads=None):
+              forced=None, nthreads=None, limits=None):
     """One CSM round over BH caches. K, V: [BH, cap, d]; N: [BH, cap]; length: [BH].
 
     Inputs are not modified. Returns dict with the new K, V, N, len, the
     per-chunk records match/sim/margin [BH, maxch, c/2] and cut [BH, maxch]
     (maxch = chunks that fit in cap), and per output row its pre-round row
     (origin [BH, cap]) and whether it is a merged centroid (merged [BH, cap]).
+    limits: optional [BH] ints; limits[u] > 0 processes only unit u's first
+    limits[u] chunks (budget-exact compression).
     """
     K, V, N, L = _f64(K).copy(), _f64(V).copy(), _i32(N).copy(), _i32(length).copy()
     BH, cap, d = K.shape
@@ -145,10 +147,11 @@ def csm_round(K, V, N, length, n1: int, n2: int, c: int, m: int, skip=None,
                origin=np.zeros((BH, cap), np.int32), merged=np.zeros((BH, cap), np.uint8))
     sk = None if skip is None else np.ascontiguousarray(np.asarray(skip, dtype=np.uint8))
     f = None if forced is None else _i32(forced)
+    lim = None if limits is None else _i32(np.asarray(limits).reshape(BH))
     rc = _load().oracle_csm_round(_ptr(K), _ptr(V), _ptr(N), _ptr(L), BH, cap, d, n1, n2, c, m,
                                   _ptr(sk), _ptr(f), _ptr(rec["match"]), _ptr(rec["sim"]),
                                   _ptr(rec["margin"]), _ptr(rec["cut"]), maxch, _ptr(rec["origin"]),
-                                  _ptr(rec["merged"]), _threads(nthreads))
+                                  _ptr(rec["merged"]), _ptr(lim), _threads(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_csm_round failed ({rc})")
     return dict(K=K, V=V, N=N, len=L, **rec)

@@ -209,12 +209,15 @@ int32_t oracle_num_chunks(int32_t s, int32_t n1, int32_t n2, int32_t c)
  * K, V: [cap][d]; N: [cap]; *len: current length s, updated.
  * Per-chunk records (may be NULL) are indexed [j][a] with row stride h=c/2
  * for up to maxch chunks.
+ * limit > 0 processes only the first (oldest) min(limit, chunks) full chunks;
+ * every later row, unprocessed chunks included, moves down unchanged
+ * (budget-exact compression; the pages' Algorithm 1 compresses every chunk).
  */
 static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
                     int32_t d, int32_t n1, int32_t n2, int32_t c, int32_t m,
                     const int32_t* forced, int32_t* match, double* sim,
                     double* margin, double* cut, int32_t maxch,
-                    int32_t* origin, uint8_t* merged)
+                    int32_t* origin, uint8_t* merged, int32_t limit)
 {
     /* origin/merged (may be NULL): [cap], per output row the pre-round row it
      * comes from and whether it is a merged centroid; identity when nothing merges */
@@ -224,8 +227,9 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
         for (int32_t t = 0; t < *len; ++t) merged[t] = 0;
     const int32_t s = *len;
     const int32_t h = c / 2;
-    const int32_t ch = oracle_num_chunks(s, n1, n2, c);
-    if (ch > maxch) return -2;
+    const int32_t ch_all = oracle_num_chunks(s, n1, n2, c);
+    if (ch_all > maxch) return -2;
+    const int32_t ch = (limit > 0 && limit < ch_all) ? limit : ch_all;
     if (ch == 0 || m == 0) return 0;
 
     /* pre-round copy of everything from the first chunk on */
@@ -263,7 +267,7 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
         w += c - m;
     }
     if (rc == 0) {
-        /* unprocessed remainder and recent window follow in order */
+        /* unprocessed chunks, remainder and recent window follow in order */
         const int32_t tail0 = ch * c; /* index into the pre-round copy */
         const int32_t tail = count - tail0;
         memcpy(K + (size_t)w * d, K0 + (size_t)tail0 * d, sizeof(double) * (size_t)tail * d);
@@ -291,6 +295,7 @@ static int csm_unit(double* K, double* V, int32_t* N, int32_t* len, int32_t cap,
  * One CSM round over BH = batch * h_kv independent caches.
  * K, V: [BH][cap][d] fp64; N: [BH][cap]; len: [BH]. skip[u] != 0 leaves unit
  * u untouched (outlier head, or a sequence not compressed this round).
+ * limits[u] > 0 (limits may be NULL) caps unit u at its first limits[u] chunks.
  * Records: match/sim/margin [BH][maxch][c/2], cut [BH][maxch], origin and
  * merged [BH][cap], all optional; forced [BH][maxch][c/2] optional. Returns 0 on success, else the first
  * failing unit's code (-1 bad forced decisions, -2 maxch too small).
@@ -300,7 +305,7 @@ int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
                      int32_t c, int32_t m, const uint8_t* skip,
                      const int32_t* forced, int32_t* match, double* sim,
                      double* margin, double* cut, int32_t maxch,
-                     int32_t* origin, uint8_t* merged, int32_t nthreads)
+                     int32_t* origin, uint8_t* merged, const int32_t* limits, int32_t nthreads)
 {
     int rc_all = 0;
     const size_t rec = (size_t)maxch * (c / 2);
@@ -321,7 +326,7 @@ int oracle_csm_round(double* K, double* V, int32_t* N, int32_t* len,
                           margin ? margin + u * rec : NULL,
                           cut ? cut + (size_t)u * maxch : NULL, maxch,
                           origin ? origin + (size_t)u * cap : NULL,
-                          merged ? merged + (size_t)u * cap : NULL);
+                          merged ? merged + (size_t)u * cap : NULL, limits ? limits[u] : 0);
         if (rc != 0) {
 #pragma omp critical
             if (rc_all == 0) rc_all = rc;

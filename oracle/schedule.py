@@ -42,6 +42,38 @@ def len_after(s: int, n1: int, n2: int, c: int, m: int) -> int:
     return s - num_chunks(s, n1, n2, c) * m
 
 
+def chunks_to_budget(s: int, B: float, n1: int, n2: int, c: int, m: int) -> int:
+    """Budget-exact compression (an extension beside the pages' Algorithm 1,
+    which merges every full chunk): the fewest oldest chunks whose merge brings
+    s to <= B. Each merged chunk removes m rows, so k = ceil((s - B) / m),
+    capped by the full chunks there are."""
+    if m <= 0 or not (float(s) > float(B)):
+        return 0
+    return min(int(math.ceil((float(s) - float(B)) / float(m))), num_chunks(s, n1, n2, c))
+
+
+def plan_budget_exact(n: int, R: float, Gamma: int, g: int, n1: int, n2: int, c: int,
+                      r_init: float = 0.5, dr: float = 0.0, r_min: float = 0.0, steps: int | None = None):
+    """As plan(), but every round merges only chunks_to_budget(...) chunks.
+
+    Returns a list of (step, s_before, r, m, k, s_after)."""
+    B = budget(n, R, Gamma)
+    s, j, out = n, 0, []
+    total = Gamma if steps is None else steps
+    for step in range(0, total + 1):
+        if step > 0:
+            s += 1
+        if should_trigger(s, B, g):
+            r = ratio(j, r_init, dr, r_min)
+            m = edges_per_chunk(r, c)
+            k = chunks_to_budget(s, B, n1, n2, c, m)
+            s2 = s - k * m
+            out.append((step, s, r, m, k, s2))
+            s = s2
+            j += 1
+    return out
+
+
 def plan(n: int, R: float, Gamma: int, g: int, n1: int, n2: int, c: int,
          r_init: float = 0.5, dr: float = 0.0, r_min: float = 0.0, steps: int | None = None):
     """Rounds of Algorithm 1 for one sequence of prefill length n.

@@ -9,12 +9,14 @@ rounds) on inputs small enough for pure Python.
 import numpy as np
 
 
-def csm_round_bruteforce(K, V, N, s, n1, n2, c, m):
+def csm_round_bruteforce(K, V, N, s, n1, n2, c, m, limit=0):
     """K, V: [s, d] float64; N: [s] ints. Returns (K', V', N', s', matches)."""
     K = np.asarray(K, float)[:s]
     V = np.asarray(V, float)[:s]
     N = [int(x) for x in N[:s]]
     n_chunks = max(0, s - n1 - n2) // c
+    if limit > 0:  # budget-exact: only the oldest `limit` chunks are matched
+        n_chunks = min(n_chunks, limit)
     if n_chunks == 0 or m == 0:
         return K.copy(), V.copy(), list(N), s, []
     rows_k, rows_v, rows_n, matches = [], [], [], []
