@@ -62,9 +62,11 @@ def csm_call_stats(w, rd, head_mask):
     active_heads = w.h_kv - int(np.asarray(head_mask).sum())
     tokens = 0
     nbytes = 0
-    for s in rd.s_before:
+    for k, s in enumerate(rd.s_before):
         mid = max(0, s - w.n1 - w.n2)
         ch = mid // w.c
+        if rd.limits and rd.limits[k] > 0:  # budget-exact round: only the oldest chunks
+            ch = min(ch, rd.limits[k])
         tail = s - (w.n1 + ch * w.c) if ch else 0
         tokens += s * w.layers
         per_head = ch * w.c * rb + ch * (w.c - rd.m) * rb + 2 * tail * rb
@@ -231,7 +233,7 @@ def run_reference(args):
     rank, world, _ = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     for _ in range(args.warmup):
         oracle_sample(w, units=args.ref_units)
     vals, secs = [], []
@@ -252,11 +254,19 @@ def run_reference(args):
     return 0
 
 
+def workload_of(args):
+    from online_kv_cache_chunked_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    return synth.scaled(w, budget_exact=True) if getattr(args, "budget_exact", False) else w
+
+
 def config_of(w):
     return {"workload": w.name, "layers": w.layers, "sequences": w.seqs, "kv_heads": w.h_kv, "q_heads": w.h_q,
             "head_dim": w.d, "prefill_tokens": list(w.n) if len(set(w.n)) > 1 else w.n[0],
             "decode_steps": w.steps, "cache_dtype": w.dtype, "n1": w.n1, "n2": w.n2, "c": w.c, "R": w.R,
             "r_init": w.r_init, "delta_r": w.dr, "r_min": w.r_min, "g": w.g, "outlier_frac": w.outlier_frac,
+            "budget_exact": w.budget_exact,
             "parallelism": "independent replicas per GPU (no collective)",
             "l2": "inputs larger than L2: each decode step reads ~1.1 GB of cache, each prefill round ~13 GB"}
 
@@ -274,7 +284,7 @@ def run_gpu(args):
     if not os.path.exists(_build.OUT):
         _build.build()
     B.load()
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     stream = torch.cuda.current_stream()
     d = synth.make_device(w)
     K0, V0, N0, L0 = (d[k].clone() for k in ("K", "V", "N", "len"))
@@ -507,6 +517,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
                     help="zero a 2xL2 buffer before every attention call (auto: when a call reads < 2xL2)")
+    ap.add_argument("--budget-exact", action="store_true",
+                    help="each round merges only the oldest chunks needed to bring s under the budget")
     ap.add_argument("--csm-kernel", default="auto", choices=sorted(CSM_KERNELS),
                     help="compression kernel: auto, simt (CUDA cores), ring or split (tensor cores)")
     args = ap.parse_args()

@@ -122,6 +122,13 @@ typedef struct {
                                  timeout and reports CSMKV_ERR_TIMEOUT (the cache is
                                  then partly compacted and must be discarded) */
     int32_t kernel;           /* which compression kernel runs (CSM_KERNEL_*) */
+    const int32_t* seq_max_chunks; /* device [batch] or NULL. Budget-exact rounds:
+                                 entry b > 0 processes only the first (oldest)
+                                 min(entry, full chunks) chunks of sequence b;
+                                 every later row, unprocessed chunks included,
+                                 moves down unchanged and len -= chunks * m.
+                                 <= 0 or NULL: every full chunk (the pages'
+                                 Algorithm 1). See csm_chunks_to_budget. */
 } csm_options;
 
 /* csm_options.kernel. AUTO picks a tensor-core kernel where the shape allows
@@ -259,6 +266,7 @@ typedef struct {
     int32_t step;            /* decode step after whose attention the round runs (>= 1) */
     double r;                /* merge ratio of the round */
     const uint8_t* seq_mask; /* device [batch], nonzero = compress; NULL = all */
+    const int32_t* seq_max_chunks; /* device [batch] or NULL: as csm_options.seq_max_chunks */
 } csm_round_plan;
 
 typedef struct {
@@ -303,6 +311,12 @@ double csm_ratio(int32_t j, double r_init, double dr, double r_min); /* max(r_in
 int32_t csm_edges_per_chunk(double r, int32_t c);                 /* floor(r c + 1e-9) */
 int64_t csm_num_chunks(int64_t s, int32_t n1, int32_t n2, int32_t c); /* floor(max(0, s-n1-n2) / c) */
 int64_t csm_len_after(int64_t s, int32_t n1, int32_t n2, int32_t c, int32_t m); /* s - chunks * m */
+/* Budget-exact compression (an extension; the pages' Algorithm 1 compresses
+ * every full chunk): the fewest oldest chunks whose merge brings s to <= B,
+ * k = ceil((s - B) / m), at most the full chunks there are; 0 when s <= B or
+ * m <= 0. After a prefill-sized round the cache then sits just under the
+ * budget, and the trigger fires again after about m appends. */
+int32_t csm_chunks_to_budget(int64_t s, double B, int32_t n1, int32_t n2, int32_t c, int32_t m);
 
 /* ------------------------------------------------------------------------
  * Device status word (offset 0 of every workspace)

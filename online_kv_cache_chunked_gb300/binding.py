@@ -35,14 +35,15 @@ class Cache(ctypes.Structure):
 
 class CsmOptions(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("withhold_signals", ctypes.c_int32),
-                ("kernel", ctypes.c_int32)]
+                ("kernel", ctypes.c_int32), ("seq_max_chunks", ctypes.c_void_p)]
 
 
 CSM_KERNEL_AUTO, CSM_KERNEL_SIMT, CSM_KERNEL_TC_RING, CSM_KERNEL_TC_SPLIT = 0, 1, 2, 3
 
 
 class CsmRoundPlan(ctypes.Structure):
-    _fields_ = [("step", ctypes.c_int32), ("r", ctypes.c_double), ("seq_mask", ctypes.c_void_p)]
+    _fields_ = [("step", ctypes.c_int32), ("r", ctypes.c_double), ("seq_mask", ctypes.c_void_p),
+                ("seq_max_chunks", ctypes.c_void_p)]
 
 
 class CsmDecodeLoop(ctypes.Structure):
@@ -86,6 +87,7 @@ _SIGS = {
     "csm_edges_per_chunk": (I32, [F64, I32]),
     "csm_num_chunks": (I64, [I64, I32, I32, I32]),
     "csm_len_after": (I64, [I64, I32, I32, I32, I32]),
+    "csm_chunks_to_budget": (I32, [I64, F64, I32, I32, I32, I32]),
     "csmkv_device_status": (ctypes.c_int, [P, P]),
     "csmkv_clear_status": (ctypes.c_int, [P, P]),
     "csmkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -164,9 +166,12 @@ def csm_compress(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, w
 
 
 def csm_compress_ex(K, V, N, length, n1, n2, c, r, head_mask=None, seq_mask=None, match_out=None,
-                    wait_timeout_ns=0, withhold_signals=0, kernel=0, workspace=None, stream=None):
+                    wait_timeout_ns=0, withhold_signals=0, kernel=0, seq_max_chunks=None, workspace=None,
+                    stream=None):
+    """seq_max_chunks: optional device int32 [batch]; entry > 0 caps that sequence's
+    round at its oldest `entry` chunks (budget-exact compression)."""
     cache = cache_desc(K)
-    opts = CsmOptions(int(wait_timeout_ns), int(withhold_signals), int(kernel))
+    opts = CsmOptions(int(wait_timeout_ns), int(withhold_signals), int(kernel), _ptr(seq_max_chunks))
     rc = load().csm_compress_ex(_ptr(K), _ptr(V), _ptr(N), _ptr(length), ctypes.byref(cache), n1, n2, c,
                                 float(r), _ptr(head_mask), _ptr(seq_mask), _ptr(match_out),
                                 ctypes.byref(opts), _ptr(workspace),
@@ -232,7 +237,8 @@ def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), 
                    attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None):
     """Decode steps first_step .. first_step+steps-1 (1-based) issued natively: per step
     append(k_new[i-1], v_new[i-1]), attention(q[i-1]) -> out[i-1], then the planned
-    rounds of that step. rounds: iterable of (step, r, seq_mask or None), sorted by step.
+    rounds of that step. rounds: iterable of (step, r, seq_mask or None[, seq_max_chunks or
+    None]), sorted by step.
     attn_events / csm_events: torch.cuda.Event lists (2 per call), recorded once before."""
     cache = cache_desc(K)
     if steps is None:
@@ -241,8 +247,10 @@ def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), 
         scale = 1.0 / (K.shape[-1] ** 0.5)
     rl = list(rounds)
     rarr = (CsmRoundPlan * max(1, len(rl)))()
-    for k, (st, r, sm) in enumerate(rl):
-        rarr[k] = CsmRoundPlan(int(st), float(r), _ptr(sm))
+    for k, rd in enumerate(rl):
+        st, r, sm = rd[:3]
+        lim = rd[3] if len(rd) > 3 else None
+        rarr[k] = CsmRoundPlan(int(st), float(r), _ptr(sm), _ptr(lim))
     ae, ce = _event_array(attn_events), _event_array(csm_events)
     nb = lambda t: t.numel() * t.element_size() if t is not None else 0  # noqa: E731
     loop = CsmDecodeLoop(_ptr(K), _ptr(V), _ptr(N), _ptr(length), cache, int(q.shape[2]), float(scale),
@@ -276,6 +284,10 @@ def csm_num_chunks(s, n1, n2, c) -> int:
 
 def csm_len_after(s, n1, n2, c, m) -> int:
     return int(load().csm_len_after(int(s), int(n1), int(n2), int(c), int(m)))
+
+
+def csm_chunks_to_budget(s, B, n1, n2, c, m) -> int:
+    return int(load().csm_chunks_to_budget(int(s), float(B), int(n1), int(n2), int(c), int(m)))
 
 
 def csmkv_device_status(workspace, stream=None) -> int:

@@ -30,6 +30,7 @@ struct CsmParams {
     int32_t* flag_v;   // [BH][L] epoch when the item's V source rows are on chip
     const uint8_t* head_mask;
     const uint8_t* seq_mask;
+    const int32_t* seq_limit;  // [batch] or NULL: at most this many chunks of sequence b (<= 0: all)
     int32_t BH, h_kv, cap, D, n1, n2, c, m, maxch, L;
     int64_t timeout_ns;
     int32_t withhold;

@@ -43,6 +43,10 @@ __global__ void __launch_bounds__(1024) csm_prologue_kernel(const CsmParams p) {
         if (active) {
             const int mid = s - p.n1 - p.n2;
             ch = mid > 0 ? mid / p.c : 0;
+            if (p.seq_limit) {  // budget-exact: only the oldest chunks; the rest moves as tail
+                const int lim = p.seq_limit[u / p.h_kv];
+                if (lim > 0 && lim < ch) ch = lim;
+            }
             if (ch > 0) tp = (s - (p.n1 + ch * p.c) + kTailRows - 1) / kTailRows;
         }
         p.unit_ch[u] = ch;
@@ -194,7 +198,9 @@ static size_t csm_layout(const csmkv_cache* cache, int32_t n1, int32_t n2, int32
                          size_t* off_ch, size_t* off_tp, size_t* off_fkn, size_t* off_fv, int32_t* L_out) {
     const size_t BH = (size_t)cache->batch * cache->h_kv;
     const int32_t maxch = csm_max_chunks(cache, n1, n2, c);
-    const int32_t tail = (c - 1 + n2 + kTailRows - 1) / kTailRows;
+    // tail pieces: the remainder and recent window, or (budget-exact rounds) every
+    // row after the processed chunks, at most the whole cache
+    const int32_t tail = (cache->cap + kTailRows - 1) / kTailRows;
     const int32_t L = maxch + tail;
     size_t off = kHeaderBytes;
     *off_snap = off;
@@ -263,6 +269,7 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     P.flag_v = reinterpret_cast<int32_t*>(ws + o_fv);
     P.head_mask = head_mask;
     P.seq_mask = seq_mask;
+    P.seq_limit = opts ? opts->seq_max_chunks : nullptr;
     P.BH = cache->batch * cache->h_kv;
     P.h_kv = cache->h_kv;
     P.cap = cache->cap;

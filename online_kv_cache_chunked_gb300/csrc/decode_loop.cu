@@ -79,6 +79,7 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
         for (; ri < L->n_rounds && L->rounds[ri].step == i; ++ri) {
             const csm_round_plan& R = L->rounds[ri];
             if ((rc = record(L->csm_events, 2 * csm_k, st)) != CSMKV_OK) return rc;
+            opts.seq_max_chunks = R.seq_max_chunks;
             rc = csm_compress_ex(L->K, L->V, L->N, L->len, &C, L->n1, L->n2, L->c, R.r, L->head_mask, R.seq_mask,
                                  nullptr, &opts, L->ws_csm, L->ws_csm_bytes, stream);
             if (rc != CSMKV_OK) return rc;

@@ -110,6 +110,13 @@ int64_t csm_len_after(int64_t s, int32_t n1, int32_t n2, int32_t c, int32_t m) {
     return s - csm_num_chunks(s, n1, n2, c) * (int64_t)m;
 }
 
+int32_t csm_chunks_to_budget(int64_t s, double B, int32_t n1, int32_t n2, int32_t c, int32_t m) {
+    if (m <= 0 || !((double)s > B)) return 0;
+    const double need = std::ceil(((double)s - B) / (double)m);
+    const int64_t have = csm_num_chunks(s, n1, n2, c);
+    return (int32_t)(need < (double)have ? (int64_t)need : have);
+}
+
 int csmkv_device_status(const void* workspace, void* stream) {
     if (!workspace) return CSMKV_ERR_WORKSPACE;
     int32_t v = 0;

@@ -8,7 +8,9 @@ r_j = r_init - j * delta_r (floored at r_min).
 
 Every length follows a closed form (each full chunk loses exactly m rows), so the
 whole schedule is planned on the host up front with the library's host helpers and
-the device is never read back. All layers of a sequence share its schedule; outlier
+the device is never read back. With `budget_exact` a round merges only the oldest
+chunks needed to bring s to <= B (csm_chunks_to_budget), so after the first rounds
+the trigger fires about every m appends instead of compressing far below B. All layers of a sequence share its schedule; outlier
 heads are never compressed and simply grow by one row per step.
 """
 from __future__ import annotations
@@ -29,6 +31,7 @@ class Round:
     seqs: tuple         # sequences (of the workload, before layer folding) compressed now
     s_before: tuple     # their compressed-head length before the round
     s_after: tuple
+    limits: tuple = ()  # budget-exact: chunks merged per sequence (empty: every full chunk)
 
 
 def plan(w) -> list:
@@ -52,10 +55,16 @@ def plan(w) -> list:
         for r, seqs in sorted(groups.items(), key=lambda kv: -kv[0]):
             m = B.csm_edges_per_chunk(r, w.c)
             before = tuple(s[i] for i in seqs)
-            for i in seqs:
-                s[i] = B.csm_len_after(s[i], w.n1, w.n2, w.c, m)
+            limits = ()
+            if w.budget_exact:
+                limits = tuple(B.csm_chunks_to_budget(s[i], Bud[i], w.n1, w.n2, w.c, m) for i in seqs)
+            for k, i in enumerate(seqs):
+                if w.budget_exact:
+                    s[i] = s[i] - limits[k] * m
+                else:
+                    s[i] = B.csm_len_after(s[i], w.n1, w.n2, w.c, m)
                 j[i] += 1
-            rounds.append(Round(step, r, m, tuple(seqs), before, tuple(s[i] for i in seqs)))
+            rounds.append(Round(step, r, m, tuple(seqs), before, tuple(s[i] for i in seqs), limits))
     return rounds
 
 
@@ -119,6 +128,17 @@ class Pipeline:
                     if b % w.seqs in rd.seqs:
                         m[b] = 1
                 self.masks.append(torch.from_numpy(m).to(dev))
+        # budget-exact: per-round chunk caps per cache sequence (layers share a sequence's)
+        self.limits = []
+        for rd in self.rounds:
+            if not rd.limits:
+                self.limits.append(None)
+                continue
+            lim = np.zeros(w.batch, np.int32)
+            cap_of = dict(zip(rd.seqs, rd.limits))
+            for b in range(w.batch):
+                lim[b] = cap_of.get(b % w.seqs, 0)
+            self.limits.append(torch.from_numpy(lim).to(dev))
         self.by_step = {}
         for k, rd in enumerate(self.rounds):
             self.by_step.setdefault(rd.step, []).append(k)
@@ -129,12 +149,13 @@ class Pipeline:
             rd = self.rounds[k]
             if hook:
                 hook("csm", rd, True)
-            if self.csm_kernel == B.CSM_KERNEL_AUTO:
+            if self.csm_kernel == B.CSM_KERNEL_AUTO and self.limits[k] is None:
                 B.csm_compress(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
                                self.masks[k], self.ws_csm, self.stream)
             else:
                 B.csm_compress_ex(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
-                                  self.masks[k], kernel=self.csm_kernel, workspace=self.ws_csm, stream=self.stream)
+                                  self.masks[k], kernel=self.csm_kernel, seq_max_chunks=self.limits[k],
+                                  workspace=self.ws_csm, stream=self.stream)
             if hook:
                 hook("csm", rd, False)
 
@@ -158,8 +179,8 @@ class Pipeline:
             self.decode_step(i, hook)
 
     def decode_plan(self):
-        """(step, r, seq_mask) of every round after prefill, in issue order."""
-        return [(rd.step, rd.r, self.masks[k]) for k, rd in enumerate(self.rounds) if rd.step >= 1]
+        """(step, r, seq_mask, seq_max_chunks) of every round after prefill, in issue order."""
+        return [(rd.step, rd.r, self.masks[k], self.limits[k]) for k, rd in enumerate(self.rounds) if rd.step >= 1]
 
     def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None):
         """Prefill round(s), then the whole decode loop issued by the library in one call."""

@@ -51,6 +51,7 @@ class Workload:
     outlier_frac: float
     seed: int
     forced_round: bool = False  # run one round regardless of the trigger (the tiny case)
+    budget_exact: bool = False  # each round merges only the oldest chunks needed to reach B
 
     @property
     def batch(self) -> int:

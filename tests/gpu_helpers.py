@@ -30,7 +30,7 @@ def skip_vector(batch, h_kv, head_mask=None, seq_mask=None):
     return sk
 
 
-def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, kernel=0, ws=None):
+def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, kernel=0, ws=None, limits=None):
     cache = B.cache_desc(K)
     maxch = max(1, B.csm_max_chunks(cache, n1, n2, c))
     match = torch.full((K.shape[0] * K.shape[1], maxch, c // 2), -2, dtype=torch.int32, device=K.device)
@@ -38,30 +38,37 @@ def gpu_round(K, V, N, L, n1, n2, c, r, head_mask=None, seq_mask=None, kernel=0,
         ws = B.new_workspace(B.csm_workspace_bytes(cache, n1, n2, c), K.device)
     hm = None if head_mask is None else torch.as_tensor(np.asarray(head_mask, np.uint8)).to(K.device)
     sm = None if seq_mask is None else torch.as_tensor(np.asarray(seq_mask, np.uint8)).to(K.device)
+    lm = None if limits is None else torch.as_tensor(np.asarray(limits, np.int32)).to(K.device)
     B.csm_compress_ex(K, V, N, L, n1, n2, c, r, head_mask=hm, seq_mask=sm, match_out=match,
-                      kernel=kernel, workspace=ws)
+                      kernel=kernel, seq_max_chunks=lm, workspace=ws)
     torch.cuda.synchronize()
     st = B.csmkv_device_status(ws)
     assert st == 0, f"device status {st}: {B.status_str(st)}"
     return match.cpu().numpy()
 
 
-def round_parity(K, V, N, L, n1, n2, c, r, dtype, head_mask=None, seq_mask=None, kernel=0, max_dev_frac=0.01):
-    """Runs one device round in place and checks it against the oracle. Returns stats."""
+def round_parity(K, V, N, L, n1, n2, c, r, dtype, head_mask=None, seq_mask=None, kernel=0, max_dev_frac=0.01,
+                 limits=None):
+    """Runs one device round in place and checks it against the oracle. Returns stats.
+    limits: optional per-sequence chunk caps (budget-exact rounds)."""
     pre = snapshot(K, V, N, L)
     m = B.csm_edges_per_chunk(r, c)
-    gm = gpu_round(K, V, N, L, n1, n2, c, r, head_mask, seq_mask, kernel)
+    gm = gpu_round(K, V, N, L, n1, n2, c, r, head_mask, seq_mask, kernel, limits=limits)
     post = snapshot(K, V, N, L)
     sk = skip_vector(K.shape[0], K.shape[1], head_mask, seq_mask)
-    free = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk)
+    ul = None if limits is None else np.repeat(np.asarray(limits, np.int32), K.shape[1])
+    free = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk, limits=ul)
     n_chunks = np.array([0 if sk[u] else oracle.num_chunks(int(pre["len"][u]), n1, n2, c)
                          for u in range(len(sk))])
+    if ul is not None:
+        n_chunks = np.where(ul > 0, np.minimum(n_chunks, ul), n_chunks)
     if m == 0:
         n_chunks[:] = 0
     dev, fails = compare.check_round(pre["K"], free, gm, n_chunks, m, n1, c)
     assert not fails, "\n".join(fails[:10])
     forced = np.where(gm >= -1, gm, -1)
-    rep = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk, forced=forced)
+    rep = oracle.csm_round(pre["K"], pre["V"], pre["N"], pre["len"], n1, n2, c, m, skip=sk, forced=forced,
+                           limits=ul)
     fails, worst = compare.compare_state(rep, pre, post, dtype)
     assert not fails, "\n".join(fails[:10])
     # unprocessed units stay bit-identical

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted([
         "csm_workspace_bytes", "csm_compress", "csm_compress_ex", "csm_max_chunks", "csm_append_workspace_bytes",
         "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "decode_attn_logn_noalloc",
-        "csm_decode_run", "csm_budget", "csm_should_trigger",
+        "csm_decode_run", "csm_budget", "csm_chunks_to_budget", "csm_should_trigger",
         "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
         "csmkv_clear_status", "csmkv_status_str"]), names
     raw = ctypes.CDLL(_build.OUT)
@@ -67,6 +67,10 @@ def test_host_helpers_match_oracle(lib):
         assert B.csm_num_chunks(s, 16, 64, 256) == osched.num_chunks(s, 16, 64, 256)
     for s in (3540, 3541):
         assert B.csm_should_trigger(s, 3476.8, 64) == oracle.should_trigger(s, 3476.8, 64)
+    for s in (0, 3476, 3477, 3541, 3604, 3605, 8321, 16384, 65536):
+        for Bud in (3476.8, 13307.2, 6753.6):
+            for m in (0, 102, 128):
+                assert B.csm_chunks_to_budget(s, Bud, 16, 64, 256, m) == osched.chunks_to_budget(s, Bud, 16, 64, 256, m)
 
 
 @pytest.mark.parametrize("name", sorted(synth.WORKLOADS))

@@ -241,3 +241,15 @@ def test_timeout_path_reports_and_recovers(cuda_lib):
     # the context is still healthy: a normal round on a fresh cache passes parity
     K, V, N, L = _random_cache(rng, 1, 2, 2304, 128, "bf16", [[2304, 2000]])
     round_parity(K, V, N, L, 16, 64, 256, 0.5, "bf16")
+
+
+@pytest.mark.parametrize("kernel", [B.CSM_KERNEL_TC_SPLIT, B.CSM_KERNEL_TC_RING, B.CSM_KERNEL_SIMT])
+def test_budget_exact_rounds(cuda_lib, kernel):
+    """Rounds capped per sequence at the oldest k chunks: the rest of each cache moves
+    down unchanged (as tail pieces, possibly many), decisions and values as the oracle."""
+    rng = np.random.default_rng(11 + kernel)
+    n1, n2, c = 16, 64, 256
+    lengths = [[80 + 9 * 256 + 77] * 3, [80 + 4 * 256 + 5] * 3, [80 + 7 * 256] * 3]
+    K, V, N, L = _random_cache(rng, 3, 3, 2688, 128, "bf16", lengths, rho=0.93, degrees=True)
+    for r, lim in [(0.5, [2, 0, 7]), (0.45, [1, 3, 100]), (0.5, [4, 1, -1])]:
+        round_parity(K, V, N, L, n1, n2, c, r, "bf16", kernel=kernel, limits=lim)

@@ -119,3 +119,47 @@ def test_decode_loop_replays_from_a_cuda_graph(cuda_lib):
         assert torch.equal(d1[k], d2[k]), k
     assert torch.equal(p1.out, p2.out)
     assert np.array_equal(d2["len"].cpu().numpy(), final_lengths(w))
+
+
+def test_budget_exact_16k_layer_in_lockstep(cuda_lib):
+    """Budget-exact schedule on the 16K layer: every round (k = ceil((s - B) / m) oldest
+    chunks) checked against the oracle on the device's own pre-round state, lengths
+    against the host plan, attention against the oracle at sampled steps."""
+    from online_kv_cache_chunked_gb300 import binding as B
+    from oracle import schedule as S
+    from tests.gpu_helpers import round_parity
+    w = synth.scaled(synth.WORKLOADS["llama_16k"], budget_exact=True, steps=300)
+    d = synth.cache_from_numpy(w, synth.make_numpy(w))
+    p = Pipeline(w, d)
+    want = S.plan_budget_exact(16384, w.R, w.steps, w.g, w.n1, w.n2, w.c, w.r_init)
+    assert [(rd.step, rd.limits[0], rd.s_after[0]) for rd in p.rounds] == [(st, k, s2) for st, _, _, _, k, s2 in want]
+    ws = B.new_workspace(B.csm_append_workspace_bytes())
+    by_step = {rd.step: rd for rd in p.rounds}
+    checks = {1, 85, 86, 213, 300}
+    for step in range(0, w.steps + 1):
+        if step > 0:
+            B.csm_append(d["K"], d["V"], d["N"], d["len"], d["k_dec"][step - 1], d["v_dec"][step - 1], workspace=ws)
+            if step in checks:
+                B.decode_attn_logn(d["q"][step - 1], d["K"], d["V"], d["N"], d["len"], p.out[step - 1], p.ws_att)
+                torch.cuda.synchronize()
+                attn_parity(d["q"][step - 1], d["K"], d["V"], d["N"], d["len"], p.out[step - 1], "bf16")
+        if step in by_step:
+            rd = by_step[step]
+            round_parity(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, "bf16", limits=list(rd.limits))
+    assert np.array_equal(d["len"].cpu().numpy(), final_lengths(w))
+    assert int(d["N"][0, 0, :int(d["len"][0, 0])].sum()) == 16384 + w.steps
+
+
+def test_budget_exact_native_loop_matches_per_call(cuda_lib):
+    w = synth.scaled(synth.WORKLOADS["llama_32k_b4"], budget_exact=True, steps=200)
+    d1 = synth.make_device(w)
+    d2 = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d1.items()}
+    p1, p2 = Pipeline(w, d1), Pipeline(w, d2)
+    assert sum(1 for rd in p1.rounds if rd.step >= 1) >= 3
+    p1.run()
+    p2.run_native()
+    torch.cuda.synchronize()
+    for k in ("K", "V", "N", "len"):
+        assert torch.equal(d1[k], d2[k]), k
+    assert torch.equal(p1.out, p2.out)
+    assert np.array_equal(d2["len"].cpu().numpy(), final_lengths(w))
