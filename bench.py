@@ -422,7 +422,9 @@ def run_gpu(args):
                             "gbs": csm_stats[k][1] / (round_ms[k] / 1e3) / 1e9}
                            for k, rd in enumerate(rounds)]},
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 * len(rounds) + ((2 if w.batch * w.h_kv <= 2048 else 3)
+        # per decode step: the fused append + attention kernel (+ its prologue beyond 2048
+        # units) and the L2 eviction read when enabled; per round: prologue + main kernel
+        "gpu_launches": args.steps * (2 * len(rounds) + ((1 if w.batch * w.h_kv <= 2048 else 2)
                                                           + (1 if flush is not None else 0)) * w.steps),
         "clocks": clocks,
     }
@@ -489,7 +491,8 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     dk.copy_(hk, non_blocking=True)
     dv.copy_(hv, non_blocking=True)
     B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], dq, dk, dv, dout, w.n1, w.n2, w.c, rounds=(),
-                     head_mask=p.head_mask, ws_csm=p.ws_csm, ws_append=p.ws_app, ws_attn=p.ws_att, steps=nsteps)
+                     head_mask=p.head_mask, ws_csm=p.ws_csm, ws_append=p.ws_app, ws_attn=p.ws_att, steps=nsteps,
+                     fused_append=True)
     ho.copy_(dout, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()

@@ -193,6 +193,25 @@ int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t*
                      void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * One fused decode step: append, then attend   [Chelsea §三 算法流程,
+ *                                               Algorithm 1 decode update]
+ * Equivalent to csm_append(k_new, v_new) followed by decode_attn_logn on the
+ * same stream, with the same results bit for bit, in one kernel for bf16: the
+ * new token's K, V row and degree 1 are written at row len of every unit by
+ * the CTA whose share of the tokens holds that row (just before it loads the
+ * row), the unit is attended with len + 1 rows, and the last CTA to finish
+ * sets len += 1. A unit with len == cap is attended unchanged and
+ * CSMKV_ERR_CAPACITY is recorded in the workspace status word. fp32 caches
+ * run the two kernels back to back.
+ * k_new, v_new: device [batch][h_kv][head_dim] in the cache dtype; K, V, N,
+ * len: device, in/out; q, out, scale, workspace as for decode_attn_logn (the
+ * same workspace size).
+ * ---------------------------------------------------------------------- */
+int decode_step_logn(const void* q, const void* k_new, const void* v_new, void* K, void* V, int32_t* N,
+                     int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale, void* out,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention without a caller-provided workspace.
  * (The pages have no counterpart: this is a deployment convenience.)
  *
@@ -296,6 +315,8 @@ typedef struct {
     void* const* csm_events;
     void* l2_flush;
     size_t l2_flush_bytes;
+    int32_t fused_append; /* nonzero: each step's append and attention run as one
+                             decode_step_logn (ws_append unused) */
 } csm_decode_loop;
 
 int csm_decode_run(const csm_decode_loop* loop, int32_t first_step, int32_t steps, void* stream);

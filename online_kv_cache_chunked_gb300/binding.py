@@ -57,7 +57,8 @@ class CsmDecodeLoop(ctypes.Structure):
                 ("ws_append", ctypes.c_void_p), ("ws_append_bytes", ctypes.c_size_t),
                 ("ws_attn", ctypes.c_void_p), ("ws_attn_bytes", ctypes.c_size_t),
                 ("attn_events", ctypes.POINTER(ctypes.c_void_p)), ("csm_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("l2_flush", ctypes.c_void_p), ("l2_flush_bytes", ctypes.c_size_t)]
+                ("l2_flush", ctypes.c_void_p), ("l2_flush_bytes", ctypes.c_size_t),
+                ("fused_append", ctypes.c_int32)]
 
 
 _lib = None
@@ -80,6 +81,7 @@ _SIGS = {
     "decode_attn_workspace_bytes": (SZ, [CP, I32]),
     "decode_attn_logn": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
     "decode_attn_logn_noalloc": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P]),
+    "decode_step_logn": (ctypes.c_int, [P, P, P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
     "csm_decode_run": (ctypes.c_int, [ctypes.POINTER(CsmDecodeLoop), I32, I32, P]),
     "csm_budget": (F64, [I64, F64, I64]),
     "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
@@ -207,6 +209,18 @@ def decode_attn_logn(q, K, V, N, length, out, workspace, scale=None, stream=None
     _check("decode_attn_logn", rc)
 
 
+def decode_step_logn(q, k_new, v_new, K, V, N, length, out, workspace, scale=None, stream=None):
+    """csm_append(k_new, v_new) then decode_attn_logn, fused into one kernel for bf16."""
+    cache = cache_desc(K)
+    h_q = q.shape[1]
+    if scale is None:
+        scale = 1.0 / (K.shape[-1] ** 0.5)
+    rc = load().decode_step_logn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V), _ptr(N), _ptr(length),
+                                 ctypes.byref(cache), h_q, float(scale), _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check("decode_step_logn", rc)
+
+
 def decode_attn_logn_noalloc(q, K, V, N, length, out, scale=None, stream=None):
     """decode_attn_logn with the library's own fixed scratch instead of a workspace,
     for callers that cannot allocate device memory."""
@@ -234,7 +248,7 @@ def _event_array(events):
 
 def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), head_mask=None,
                    ws_csm=None, ws_append=None, ws_attn=None, first_step=1, steps=None, csm_kernel=0,
-                   attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None):
+                   attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None, fused_append=False):
     """Decode steps first_step .. first_step+steps-1 (1-based) issued natively: per step
     append(k_new[i-1], v_new[i-1]), attention(q[i-1]) -> out[i-1], then the planned
     rounds of that step. rounds: iterable of (step, r, seq_mask or None[, seq_max_chunks or
@@ -256,7 +270,7 @@ def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), 
     loop = CsmDecodeLoop(_ptr(K), _ptr(V), _ptr(N), _ptr(length), cache, int(q.shape[2]), float(scale),
                          _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), int(n1), int(n2), int(c), _ptr(head_mask),
                          int(csm_kernel), rarr, len(rl), _ptr(ws_csm), nb(ws_csm), _ptr(ws_append), nb(ws_append),
-                         _ptr(ws_attn), nb(ws_attn), ae, ce, _ptr(l2_flush), nb(l2_flush))
+                         _ptr(ws_attn), nb(ws_attn), ae, ce, _ptr(l2_flush), nb(l2_flush), int(bool(fused_append)))
     rc = load().csm_decode_run(ctypes.byref(loop), int(first_step), int(steps), _stream(stream))
     _check("csm_decode_run", rc)
 

@@ -39,6 +39,14 @@ constexpr int kMaxScanUnits = 2048;  // units whose offsets a CTA scans itself
 struct DecParams {
     const void* q;
     const int32_t* len;
+    // fused append (k_new != NULL): every unit's new token is written at row len and
+    // attended, and len grows by one at the end of the call
+    const void* k_new;    // [BH][D]
+    const void* v_new;    // [BH][D]
+    void* K;
+    void* V;
+    int32_t* N;
+    int32_t* len_rw;      // the same array as len
     void* out;
     WsHeader* hdr;
     int32_t* prefix;      // [BH + 1] token offset of every unit
@@ -52,6 +60,21 @@ struct DecParams {
     float scale;          // natural-log scale (fp32 path)
 };
 
+// Rows of unit u this call attends: len, plus the appended token in fused-append
+// mode (a full unit records CSMKV_ERR_CAPACITY and is attended as it is).
+__device__ __forceinline__ int eff_len(const DecParams& p, int u, bool record) {
+    int v = p.len[u];
+    if (v < 0 || v > p.cap) {
+        if (record) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+        return 0;
+    }
+    if (p.k_new) {
+        if (v < p.cap) ++v;
+        else if (record) record_status(&p.hdr->status, CSMKV_ERR_CAPACITY);
+    }
+    return v;
+}
+
 // ----------------------------------------------------------------------------
 // Prologue (one CTA): prefix sums of the lengths, tokens per CTA, first unit of
 // every CTA's range.
@@ -63,14 +86,7 @@ __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p
     __syncthreads();
     for (int base = 0; base < p.BH; base += 1024) {
         const int u = base + tid;
-        int v = 0;
-        if (u < p.BH) {
-            v = p.len[u];
-            if (v < 0 || v > p.cap) {
-                record_status(&p.hdr->status, CSMKV_ERR_ARG);
-                v = 0;
-            }
-        }
+        const int v = u < p.BH ? eff_len(p, u, true) : 0;
         int incl = v;
         for (int o = 1; o < 32; o <<= 1) {
             const int x = __shfl_up_sync(0xffffffffu, incl, o);
@@ -164,6 +180,7 @@ struct DecSmall {
     uint64_t empty[kStages];
     int abort_flag;
     int last;      // this CTA is the last contributor of the unit being closed
+    int bump;      // fused append: this CTA finished last and bumps the lengths
     int u0;        // first unit of the CTA's range
     int total;
     int warp_tot[kDecThreads / 32];
@@ -309,14 +326,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         int local = 0;
         for (int i = 0; i < per; ++i) {
             const int u = ub + i;
-            if (u < p.BH) {
-                int v = p.len[u];
-                if (v < 0 || v > p.cap) {
-                    record_status(&p.hdr->status, CSMKV_ERR_ARG);
-                    v = 0;
-                }
-                local += v;
-            }
+            if (u < p.BH) local += eff_len(p, u, true);
         }
         int incl = local;
         for (int o = 1; o < 32; o <<= 1) {
@@ -341,8 +351,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             const int u = ub + i;
             if (u < p.BH) {
                 sPrefix[u] = run;
-                const int v = p.len[u];
-                run += (v < 0 || v > p.cap) ? 0 : v;
+                run += eff_len(p, u, false);
             }
         }
         __syncthreads();
@@ -366,7 +375,23 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
     const int r0 = blockIdx.x * W;
     const int r1 = min(total, r0 + W);
-    if (r0 >= r1) return;
+    // Fused append: once every CTA is done (and so done reading len), the last one
+    // moves every unit's length past its new token.
+    auto finish_append = [&](int nthr, bool block_sync) {
+        if (!p.k_new) return;
+        if (tid == 0) sm.bump = atomicAdd(&p.hdr->ctas_done, 1) == (int)gridDim.x - 1;
+        if (block_sync) __syncthreads(); else consumer_barrier();
+        if (!sm.bump) return;
+        for (int u = tid; u < p.BH; u += nthr) {
+            const int v = p.len[u];
+            if (v >= 0 && v < p.cap) p.len_rw[u] = v + 1;
+        }
+        if (tid == 0) p.hdr->ctas_done = 0;
+    };
+    if (r0 >= r1) {
+        finish_append(kDecThreads, true);
+        return;
+    }
     int u0;
     if constexpr (SCAN) {
         if (tid == 0) sm.u0 = p.BH;
@@ -378,7 +403,28 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     } else {
         u0 = p.cta_unit[blockIdx.x];
     }
+    int u0_last = u0;  // unit holding the range's last token
+    if (p.k_new)
+        while (u0_last + 1 < p.BH && pre[u0_last + 1] < r1) ++u0_last;
 
+    // Fused append: the CTA whose range holds a unit's last row (the new token)
+    // writes that row before any of its loads, 2 * D / 8 sixteen-byte pieces per
+    // unit spread over the block; the fence orders the writes before the TMA reads.
+    if (p.k_new) {
+        constexpr int PPR = D / 8;  // 16-byte pieces per row
+        for (int i = tid; i < (u0_last - u0 + 1) * 2 * PPR; i += kDecThreads) {
+            const int u = u0 + i / (2 * PPR), k = i % (2 * PPR);
+            const int old = p.len[u];
+            if (old < 0 || old >= p.cap || pre[u + 1] - 1 < r0 || pre[u + 1] - 1 >= r1) continue;
+            const size_t r = (size_t)u * p.cap + old;
+            const bool isv = k >= PPR;
+            const uint4* src = static_cast<const uint4*>(isv ? p.v_new : p.k_new) + (size_t)u * PPR + (k % PPR);
+            uint4* dst = static_cast<uint4*>(isv ? p.V : p.K) + r * PPR + (k % PPR);
+            *dst = *src;
+            if (k == 0) p.N[r] = 1;
+            fence_proxy_async_global();
+        }
+    }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -629,6 +675,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         consumer_barrier();  // sm.last is rewritten for the next unit
     }
     if (!ok && tid == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
+    finish_append(kConsumerWarps * 32, false);
 }
 
 // ----------------------------------------------------------------------------
@@ -740,12 +787,16 @@ extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t 
     return dec_layout(cache, nCTA, &a, &b, &c, &d, &e, &f);
 }
 
-extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
-                                const csmkv_cache* cache, int32_t h_q, float scale, void* out, void* workspace,
-                                size_t ws_bytes, void* stream) {
+// Attention over the cache, optionally with the step's new token appended first
+// (k_new != NULL: bf16 fuses the append into the attention kernel).
+static int decode_attn_impl(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                            const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
+                            void* out, void* workspace, size_t ws_bytes, void* stream) {
     int rc = check_cache(cache);
     if (rc != CSMKV_OK) return rc;
     if (!q || !K || !V || !N || !len || !out) return CSMKV_ERR_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return CSMKV_ERR_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return CSMKV_ERR_ALIGN;
     if (h_q < 1 || (h_q % cache->h_kv) != 0) return CSMKV_ERR_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return CSMKV_ERR_ARG;
     if (!aligned16(K) || !aligned16(V) || !aligned16(N) || !aligned16(q) || !aligned16(out) ||
@@ -765,6 +816,12 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
     DecParams P{};
     P.q = q;
     P.len = len;
+    P.k_new = k_new;
+    P.v_new = v_new;
+    P.K = const_cast<void*>(K);
+    P.V = const_cast<void*>(V);
+    P.N = const_cast<int32_t*>(N);
+    P.len_rw = const_cast<int32_t*>(len);
     P.out = out;
     P.hdr = reinterpret_cast<WsHeader*>(ws);
     P.prefix = reinterpret_cast<int32_t*>(ws + o_prefix);
@@ -784,6 +841,12 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
     P.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    if (!bf16 && k_new) {  // fp32: the append kernel, then attention (status in this workspace)
+        rc = csm_append(const_cast<void*>(K), const_cast<void*>(V), const_cast<int32_t*>(N), const_cast<int32_t*>(len),
+                        cache, k_new, v_new, nullptr, workspace, ws_bytes, stream);
+        if (rc != CSMKV_OK) return rc;
+        P.k_new = P.v_new = nullptr;
+    }
     if (!bf16) {
         decode_f32_kernel<<<cache->batch * h_q, 128, 0, st>>>(P, static_cast<const float*>(K),
                                                               static_cast<const float*>(V), N);
@@ -813,4 +876,17 @@ extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, con
     decode_prologue_kernel<<<1, 1024, 0, st>>>(P);
     if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
     return D == 128 ? launch_decode_bf16<128, false>(P, tk, tv, tn, st) : launch_decode_bf16<64, false>(P, tk, tv, tn, st);
+}
+
+extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                                const csmkv_cache* cache, int32_t h_q, float scale, void* out, void* workspace,
+                                size_t ws_bytes, void* stream) {
+    return decode_attn_impl(q, K, V, N, len, nullptr, nullptr, cache, h_q, scale, out, workspace, ws_bytes, stream);
+}
+
+extern "C" int decode_step_logn(const void* q, const void* k_new, const void* v_new, void* K, void* V, int32_t* N,
+                                int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale, void* out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    if (!k_new || !v_new) return CSMKV_ERR_ARG;
+    return decode_attn_impl(q, K, V, N, len, k_new, v_new, cache, h_q, scale, out, workspace, ws_bytes, stream);
 }

@@ -59,10 +59,12 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
     int attn_k = 0, csm_k = 0;
     for (int i = first_step; i < first_step + steps; ++i) {
         const size_t s = (size_t)(i - 1);
-        rc = csm_append(L->K, L->V, L->N, L->len, &C, static_cast<const uint8_t*>(L->k_new) + s * kv_step,
-                        static_cast<const uint8_t*>(L->v_new) + s * kv_step, nullptr, L->ws_append,
-                        L->ws_append_bytes, stream);
-        if (rc != CSMKV_OK) return rc;
+        const uint8_t* const kn = static_cast<const uint8_t*>(L->k_new) + s * kv_step;
+        const uint8_t* const vn = static_cast<const uint8_t*>(L->v_new) + s * kv_step;
+        if (!L->fused_append) {
+            rc = csm_append(L->K, L->V, L->N, L->len, &C, kn, vn, nullptr, L->ws_append, L->ws_append_bytes, stream);
+            if (rc != CSMKV_OK) return rc;
+        }
         if (L->l2_flush) {
             l2_evict_kernel<<<4 * csmkv::sm_count(), 256, 0, st>>>(static_cast<const uint4*>(L->l2_flush),
                                                                    L->l2_flush_bytes / 16,
@@ -70,9 +72,13 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
             if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
         }
         if ((rc = record(L->attn_events, 2 * attn_k, st)) != CSMKV_OK) return rc;
-        rc = decode_attn_logn(static_cast<const uint8_t*>(L->q) + s * q_step, L->K, L->V, L->N, L->len, &C, L->h_q,
-                              L->scale, static_cast<uint8_t*>(L->out) + s * q_step, L->ws_attn, L->ws_attn_bytes,
-                              stream);
+        const uint8_t* const qs = static_cast<const uint8_t*>(L->q) + s * q_step;
+        uint8_t* const os = static_cast<uint8_t*>(L->out) + s * q_step;
+        rc = L->fused_append
+                 ? decode_step_logn(qs, kn, vn, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
+                                    L->ws_attn_bytes, stream)
+                 : decode_attn_logn(qs, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
+                                    L->ws_attn_bytes, stream);
         if (rc != CSMKV_OK) return rc;
         if ((rc = record(L->attn_events, 2 * attn_k + 1, st)) != CSMKV_OK) return rc;
         ++attn_k;

@@ -23,7 +23,8 @@ struct WsHeader {
     int32_t levels_tail;  // CSM: max tail pieces over active units
     int32_t total_tokens; // decode: tokens over all units
     int32_t tokens_per_cta;
-    int32_t pad[57];
+    int32_t ctas_done;    // decode with append: CTAs finished; the last one bumps the lengths
+    int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 

@@ -182,8 +182,9 @@ class Pipeline:
         """(step, r, seq_mask, seq_max_chunks) of every round after prefill, in issue order."""
         return [(rd.step, rd.r, self.masks[k], self.limits[k]) for k, rd in enumerate(self.rounds) if rd.step >= 1]
 
-    def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None):
-        """Prefill round(s), then the whole decode loop issued by the library in one call."""
+    def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None, fused=True):
+        """Prefill round(s), then the whole decode loop issued by the library in one call
+        (fused: each step's append and attention as one kernel)."""
         d, w = self.d, self.w
         self.compress_at(0, hook)
         n = w.steps if steps is None else steps
@@ -191,4 +192,4 @@ class Pipeline:
                          w.c, rounds=self.decode_plan(), head_mask=self.head_mask, ws_csm=self.ws_csm,
                          ws_append=self.ws_app, ws_attn=self.ws_att, first_step=1, steps=n,
                          csm_kernel=self.csm_kernel, attn_events=attn_events, csm_events=csm_events,
-                         l2_flush=l2_flush, stream=self.stream)
+                         l2_flush=l2_flush, stream=self.stream, fused_append=fused)

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert names == sorted([
         "csm_workspace_bytes", "csm_compress", "csm_compress_ex", "csm_max_chunks", "csm_append_workspace_bytes",
-        "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "decode_attn_logn_noalloc",
+        "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "decode_attn_logn_noalloc", "decode_step_logn",
         "csm_decode_run", "csm_budget", "csm_chunks_to_budget", "csm_should_trigger",
         "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
         "csmkv_clear_status", "csmkv_status_str"]), names

@@ -164,3 +164,43 @@ def test_repeated_calls_on_one_workspace(cuda_lib):
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
     attn_parity(q, K, V, N, L, outs[0], "bf16")
+
+
+@pytest.mark.parametrize("batch,h_kv,G,cap,D,dtype", [(2, 8, 4, 1024, 128, torch.bfloat16),
+                                                       (3, 4, 7, 640, 64, torch.bfloat16),
+                                                       (300, 8, 4, 72, 128, torch.bfloat16),   # > 2048 units
+                                                       (2, 2, 2, 256, 128, torch.float32)])
+def test_fused_step_matches_append_then_attention(cuda_lib, batch, h_kv, G, cap, D, dtype):
+    """decode_step_logn = csm_append + decode_attn_logn, bit for bit: caches, lengths,
+    outputs and the status word (a full unit is attended unchanged, CAPACITY recorded)."""
+    rng = np.random.default_rng(batch * 100 + D)
+    lengths = rng.integers(0, cap, (batch, h_kv))
+    lengths[0, 0] = cap          # full: no append, CAPACITY
+    lengths[-1, -1] = 0          # empty before the append
+    q, K, V, N, L = _case(rng, batch, h_kv, G, cap, D, lengths.tolist(), dtype=dtype)
+    kn = torch.randn(batch, h_kv, D, device="cuda").to(dtype)
+    vn = torch.randn(batch, h_kv, D, device="cuda").to(dtype)
+    K2, V2, N2, L2 = K.clone(), V.clone(), N.clone(), L.clone()
+    cache = B.cache_desc(K)
+    ws_a = B.new_workspace(B.csm_append_workspace_bytes())
+    ws1 = B.new_workspace(B.decode_attn_workspace_bytes(cache, q.shape[1]))
+    ws2 = B.new_workspace(B.decode_attn_workspace_bytes(cache, q.shape[1]))
+    o1 = torch.empty(batch, h_kv * G, D, dtype=dtype, device="cuda")
+    o2 = torch.empty_like(o1)
+    B.csm_append(K, V, N, L, kn, vn, workspace=ws_a)
+    B.decode_attn_logn(q, K, V, N, L, o1, ws1)
+    for _ in range(2):  # the second call shows the per-call state resets (and appends again)
+        B.decode_step_logn(q, kn, vn, K2, V2, N2, L2, o2, ws2)
+        if _ == 0:
+            torch.cuda.synchronize()
+            assert B.csmkv_device_status(ws2) == 4  # CSMKV_ERR_CAPACITY
+            for a, b in ((K, K2), (V, V2), (N, N2), (L, L2)):
+                # NaN garbage past the lengths compares unequal to itself: compare bytes
+                assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                                   b.view(torch.uint8) if b.dtype != torch.int32 else b)
+            assert torch.equal(o1.view(torch.uint8), o2.view(torch.uint8))
+            attn_parity(q, K2, V2, N2, L2, o2, "bf16" if dtype == torch.bfloat16 else "f32")
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws_a) == 4
+    exp = np.minimum(lengths + 2, cap)
+    assert np.array_equal(L2.cpu().numpy(), exp)
