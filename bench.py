@@ -86,8 +86,9 @@ def source_sha(files):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel, key):
-    """ncu DRAM bytes (per launch or per step) of a kernel, if taken on the current source."""
+def traffic_record(kernel, key, w):
+    """ncu DRAM bytes (per launch or per step) of a kernel, if taken on the current source
+    and on this workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -98,6 +99,7 @@ def traffic_record(kernel, key):
         ok = rec.get("source_sha") == source_sha(rec.get("files", []))
     except OSError:
         ok = False
+    ok = ok and rec.get("workload_name") == w.name and not w.budget_exact
     return rec.get(key) if ok else None
 
 
@@ -410,10 +412,10 @@ def run_gpu(args):
                         "avg_call_us": 1e6 * avg_launch_s},
         "roofline": {"bound": "hbm", "achieved": per_launch_bytes / avg_launch_s / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": per_launch_bytes / avg_launch_s / 1e9 / hbm,
-                     "traffic": traffic_record("decode_attn", "bytes_per_launch"), "kernel": "decode_attn_logn",
+                     "traffic": traffic_record("decode_attn", "bytes_per_launch", w), "kernel": "decode_attn_logn",
                      "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
         "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
-                         "traffic": traffic_record("csm_compress", "bytes_per_step"), "kernel": "csm_compress",
+                         "traffic": traffic_record("csm_compress", "bytes_per_step", w), "kernel": "csm_compress",
                          "csm_kernel": args.csm_kernel,
                          "peak_kind": kind, "bytes_per_step": csm_bytes_step},
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
