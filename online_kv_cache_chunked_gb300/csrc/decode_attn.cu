@@ -35,6 +35,15 @@ constexpr int kStages = 3;
 constexpr int kDecCtasPerSm = 2;
 constexpr int kSlotHeads = 8;  // partial records are padded to 8 heads
 constexpr int kMaxScanUnits = 2048;  // units whose offsets a CTA scans itself
+constexpr int kMinTokensPerCta = 512;  // small calls use fewer CTAs (the rest exit at once)
+
+// Tokens per CTA for `total` tokens on a grid of n CTAs: an equal share, but at
+// least kMinTokensPerCta, so a small call does not spread a few tiles over
+// hundreds of CTAs and then merge hundreds of partial records.
+__host__ __device__ __forceinline__ int tokens_per_cta(int total, int n) {
+    const int share = (total + n - 1) / n;
+    return share > kMinTokensPerCta ? share : kMinTokensPerCta;
+}
 
 struct DecParams {
     const void* q;
@@ -112,7 +121,7 @@ __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p
     }
     const int total = carry_s;
     if (tid == 0) p.prefix[p.BH] = total;
-    const int W = max(1, (total + p.nCTA - 1) / p.nCTA);
+    const int W = tokens_per_cta(total, p.nCTA);
     if (tid == 0) {
         p.hdr->total_tokens = total;
         p.hdr->tokens_per_cta = W;
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         __syncthreads();
         pre = sPrefix;
         total = sm.total;
-        W = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+        W = tokens_per_cta(total, (int)gridDim.x);
     } else {
         pre = p.prefix;
         total = p.hdr->total_tokens;
