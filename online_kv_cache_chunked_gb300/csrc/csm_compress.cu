@@ -27,6 +27,7 @@ namespace csmkv {
 // ----------------------------------------------------------------------------
 // Prologue: snapshot lengths, count the items of every unit, advance the epoch.
 __global__ void __launch_bounds__(1024) csm_prologue_kernel(const CsmParams p) {
+    griddep_launch_dependents();  // the main kernel may set itself up meanwhile
     __shared__ int red[2][32];
     int mch = 0, mtp = 0;
     for (int u = threadIdx.x; u < p.BH; u += blockDim.x) {

@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
     tc_fence_after();
     const uint32_t tmem = st.tmem;
 
+    // Everything above is private setup; from here on the prologue's tables and the
+    // cache are read, so wait for the prologue (launched just before) to complete.
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t epoch = p.hdr->epoch;
     const int levels_ch = p.hdr->levels_ch, levels_tail = p.hdr->levels_tail;
     const long long total = (long long)(levels_ch + levels_tail) * BH;
@@ -387,7 +391,9 @@ int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint
     if (grid <= 0) return CSMKV_ERR_CUDA;
     auto run = [&](auto kern, int smem) {
         if (set_kernel_smem((const void*)kern, smem, true) != CSMKV_OK) return (int)CSMKV_ERR_CUDA;
-        kern<<<grid, kTc3Threads, smem, st>>>(P, tmK, tmV, tmN, tmKs, tmVs);
+        if (launch_overlapped(kern, dim3(grid), dim3(kTc3Threads), (size_t)smem, st, P, tmK, tmV, tmN, tmKs,
+                              tmVs) != cudaSuccess)
+            return (int)CSMKV_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? (int)CSMKV_OK : (int)CSMKV_ERR_CUDA;
     };
     return D == 128 ? run(csm_tc3_kernel<128>, Tc3<128>::kSmem) : run(csm_tc3_kernel<64>, Tc3<64>::kSmem);

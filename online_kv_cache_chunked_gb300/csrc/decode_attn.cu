@@ -88,6 +88,7 @@ __device__ __forceinline__ int eff_len(const DecParams& p, int u, bool record) {
 // Prologue (one CTA): prefix sums of the lengths, tokens per CTA, first unit of
 // every CTA's range.
 __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p) {
+    griddep_launch_dependents();  // the main kernel may set itself up meanwhile
     __shared__ int wsum[32];
     __shared__ int carry_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -325,6 +326,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     volatile int* const abort_flag = &sm.abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // Private setup first; then wait for the previous kernel in the stream (its
+    // lengths, cache rows and workspace state) before reading anything.
+    if (tid == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmN);
+    }
+    griddep_launch_dependents();
+    griddep_wait();
 
     // ---------------------------------------------------------------- unit offsets
     const int* pre;
@@ -780,7 +791,8 @@ static int launch_decode_bf16(const DecParams& P, const CUtensorMap& tk, const C
     static_assert(kDecCtasPerSm * (smem + 1024) <= 228 * 1024, "two CTAs per SM must fit in shared memory");
     auto kern = decode_main_kernel<D, SCAN>;
     if (set_kernel_smem((const void*)kern, smem) != CSMKV_OK) return CSMKV_ERR_CUDA;
-    kern<<<P.nCTA, kDecThreads, smem, st>>>(P, tk, tv, tn);
+    if (launch_overlapped(kern, dim3(P.nCTA), dim3(kDecThreads), (size_t)smem, st, P, tk, tv, tn) != cudaSuccess)
+        return CSMKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
 }
 

@@ -7,10 +7,30 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/csmkv.h"
 
 namespace csmkv {
+
+// Launches a kernel that may overlap its setup with the tail of the previous
+// kernel in the stream (programmatic dependent launch); the kernel must call
+// griddep_wait() before it touches memory that earlier work writes.
+template <typename... ExpTypes, typename... ActTypes>
+inline cudaError_t launch_overlapped(void (*kern)(ExpTypes...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, ActTypes&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<ActTypes>(args)...);
+}
 
 constexpr size_t kHeaderBytes = 256;  // every workspace starts with this header
 
