@@ -13,8 +13,9 @@
 //   shared selection tables; then the K output; then V through the same slot.
 // Output: when m = c/2 every A row merges and the output rows are exactly the
 // B rows, already in shared memory in the layout a 2-D TMA store takes, so the
-// merged rows are rewritten in place and two TMA stores write the block; other
-// m go through per-piece copies and merges. Three independent CTAs per SM
+// merged rows are rewritten in place and two TMA stores write the block; for
+// other m the output rows (copies and merges) are written straight to global
+// memory. Three independent CTAs per SM
 // overlap one another's loads, barriers and compute.
 // In-place safety: every item publishes an epoch-tagged "loaded" flag per array
 // once its TMA lands; an item writes an array only after the items whose source
@@ -96,9 +97,6 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
     uint32_t phase = 0, mma_phase = 0;
     bool load_pend = false, mma_pend = false, stores_pend = false;  // thread 0
 
-    auto piece = [&](int q, int cc) {
-        return slot + ((q & 1) * R::kBoxes + (cc >> 3)) * 16384 + sw128_off((uint32_t)(q >> 1), (uint32_t)(cc & 7));
-    };
     auto load_slot = [&](const CUtensorMap* map, long long g0, bool with_degrees) {  // thread 0
         mbar_expect_tx(&st.bar, (uint32_t)(R::kSlotBytes + (with_degrees ? R::kNBytes : 0)));
         const int ya = (int)(g0 & 1), za = (int)(g0 >> 1);
@@ -163,6 +161,65 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             }
             *d0 = Elem<T>::pack(acc0);
             *d1 = Elem<T>::pack(acc1);
+        }
+    };
+    // m < H: the c - m output rows (copies, or merged B rows) written straight to
+    // global memory; as merge_inplace, two 16-byte pieces per thread in a
+    // bank-distinct order, so the per-row lookups are paid once per 32 bytes.
+    auto emit_rows2 = [&](T* dst_rows, const int32_t* sN) {
+        constexpr int TPR = 4 * R::kBoxes;
+        const int sub = tid % TPR;
+        const int box = sub >> 2;
+        const uint32_t c0 = (uint32_t)((sub & 3) * 2 + (box & 1)), c1 = c0 ^ 1u;
+        uint8_t* const abox = slot + box * 16384;
+        const int n = (c - m) * TPR;
+        for (int i = tid; i < n; i += kTc3Threads) {
+            const int pr = i / TPR;
+            const int q = sm.src[pr], row = q >> 1;
+            const uint8_t* const src = slot + ((q & 1) * R::kBoxes + box) * 16384 + row * 128;
+            const uint32_t x = (uint32_t)(row & 7);
+            uint4 v0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ x) << 4));
+            uint4 v1 = *reinterpret_cast<const uint4*>(src + ((c1 ^ x) << 4));
+            if (q & 1) {
+                const float inv = sm.ninv[row];
+                if (inv != 0.0f) {  // a B row with incoming edges: degree-weighted mean
+                    float acc0[8], acc1[8], f[8];
+                    const float nb = (float)sN[q];
+                    Elem<T>::unpack(v0, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc0[e] = nb * f[e];
+                    Elem<T>::unpack(v1, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc1[e] = nb * f[e];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t bits = sm.mask[row][w];
+                        while (bits) {
+                            const int a = w * 32 + __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            const uint8_t* const arow = abox + a * 128;
+                            const uint32_t xa = (uint32_t)(a & 7);
+                            const float na = (float)sN[2 * a];
+                            Elem<T>::unpack(*reinterpret_cast<const uint4*>(arow + ((c0 ^ xa) << 4)), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc0[e] = fmaf(na, f[e], acc0[e]);
+                            Elem<T>::unpack(*reinterpret_cast<const uint4*>(arow + ((c1 ^ xa) << 4)), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc1[e] = fmaf(na, f[e], acc1[e]);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc0[e] *= inv;
+                        acc1[e] *= inv;
+                    }
+                    v0 = Elem<T>::pack(acc0);
+                    v1 = Elem<T>::pack(acc1);
+                }
+            }
+            uint4* const drow = reinterpret_cast<uint4*>(dst_rows + (size_t)pr * D) + box * 8;
+            drow[c0] = v0;
+            drow[c1] = v1;
         }
     };
     auto store_b_rows = [&](const CUtensorMap* map, long long row) {  // thread 0
@@ -318,7 +375,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
                 __syncthreads();
                 if (tid == 0) store_b_rows(&tmKs, (long long)urow + dst_row);
             } else {
-                emit_rows<T>(Kg + (urow + dst_row) * D, c - m, D, m, sm, sN, piece);
+                emit_rows2(Kg + (urow + dst_row) * D, sN);
             }
             emit_degrees(p.N + urow + dst_row, c - m, m, sm, sN);
 
@@ -347,7 +404,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
                 __syncthreads();
                 if (tid == 0) store_b_rows(&tmVs, (long long)urow + dst_row);
             } else {
-                emit_rows<T>(Vg + (urow + dst_row) * D, c - m, D, m, sm, sN, piece);
+                emit_rows2(Vg + (urow + dst_row) * D, sN);
             }
         } else {
             // ================================================================ tail piece
