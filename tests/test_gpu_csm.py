@@ -5,6 +5,7 @@ import torch
 
 from online_kv_cache_chunked_gb300 import binding as B
 from online_kv_cache_chunked_gb300 import synth
+from oracle import compare
 from tests.gpu_helpers import round_parity, snapshot, gpu_round, to64
 
 pytestmark = pytest.mark.gpu
@@ -253,3 +254,45 @@ def test_budget_exact_rounds(cuda_lib, kernel):
     K, V, N, L = _random_cache(rng, 3, 3, 2688, 128, "bf16", lengths, rho=0.93, degrees=True)
     for r, lim in [(0.5, [2, 0, 7]), (0.45, [1, 3, 100]), (0.5, [4, 1, -1])]:
         round_parity(K, V, N, L, n1, n2, c, r, "bf16", kernel=kernel, limits=lim)
+
+
+@pytest.mark.parametrize("kernel", [B.CSM_KERNEL_TC_SPLIT, B.CSM_KERNEL_SIMT])
+def test_many_short_units(cuda_lib, kernel):
+    """3000 (sequence, head) units of 0-4 chunks each: the prologue walks more units
+    than it has threads, the ticket space is wide and mostly tail pieces. Lengths and
+    degree sums on every unit; sampled units against the oracle (replaying the
+    device's decisions)."""
+    import oracle
+    rng = np.random.default_rng(17 + kernel)
+    batch, h_kv, cap, D, n1, n2, c, m = 750, 4, 1104, 128, 16, 64, 256, 128
+    lengths = rng.integers(0, cap + 1, (batch, h_kv))
+    K, V, N, L = _random_cache(rng, batch, h_kv, cap, D, "bf16", lengths.tolist(), rho=0.9, degrees=True)
+    seq_on = (rng.random(batch) < 0.8).astype(np.uint8)
+    K0, V0, N0, L0 = K.clone(), V.clone(), N.clone(), L.clone()
+    gm = gpu_round(K, V, N, L, n1, n2, c, 0.5, kernel=kernel, seq_mask=seq_on)
+    BH = batch * h_kv
+    s_pre = L0.view(BH).cpu().numpy()
+    s_post = L.view(BH).cpu().numpy()
+    rows = torch.arange(cap, device="cuda")[None, :]
+    sum_pre = (N0.view(BH, cap) * (rows < L0.view(BH, 1))).sum(dim=1).cpu().numpy()
+    sum_post = (N.view(BH, cap) * (rows < L.view(BH, 1))).sum(dim=1).cpu().numpy()
+    for u in range(BH):
+        s = int(s_pre[u])
+        want = s - oracle.num_chunks(s, n1, n2, c) * m if seq_on[u // h_kv] else s
+        assert int(s_post[u]) == want, u
+    assert np.array_equal(sum_pre, sum_post)
+    Kf, Vf, Nf = K.view(BH, cap, D), V.view(BH, cap, D), N.view(BH, cap)
+    K0f, V0f, N0f = K0.view(BH, cap, D), V0.view(BH, cap, D), N0.view(BH, cap)
+    for u in rng.choice(BH, 48, replace=False):
+        s, got = int(s_pre[u]), int(s_post[u])
+        if got == s:  # masked out or no full chunk: untouched
+            assert torch.equal(Kf[u, :s], K0f[u, :s]) and torch.equal(Vf[u, :s], V0f[u, :s])
+            continue
+        forced = np.where(gm[u:u + 1] >= -1, gm[u:u + 1], -1)
+        ref = oracle.csm_round(to64(K0f[u:u + 1]), to64(V0f[u:u + 1]), N0f[u:u + 1].cpu().numpy(),
+                               np.array([s], np.int32), n1, n2, c, m, forced=forced)
+        assert int(ref["len"][0]) == got
+        assert np.array_equal(ref["N"][0, :got], Nf[u, :got].cpu().numpy())
+        for name, T in (("K", Kf), ("V", Vf)):
+            r = ref[name][0, :got]
+            assert np.all(np.abs(r - to64(T[u, :got])) <= compare.value_tol(r, "bf16"))
