@@ -163,7 +163,7 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def oracle_sample(w, units=16, threads=None):
+def oracle_sample(w, units=16, threads=None, decode=False):
     """The fp64 oracle's prefill CSM round on a bounded sample of the workload's units
     (the first 2 layers' 16 KV heads, generated with the same recipe); tokens/s."""
     import oracle
@@ -188,12 +188,29 @@ def oracle_sample(w, units=16, threads=None):
     m = oracle.edges_per_chunk(w.r_init, w.c)
     nth = oracle.max_threads() if threads is None else threads
     t0 = time.perf_counter()
-    oracle.csm_round(K, V, N, L, ws.n1, ws.n2, ws.c, m, nthreads=nth)
+    out = oracle.csm_round(K, V, N, L, ws.n1, ws.n2, ws.c, m, nthreads=nth)
     dt = time.perf_counter() - t0
     tokens = n * layers  # tokens per (layer, sequence) cache, all KV heads
-    return dict(value=tokens / dt, unit="tokens/s", cores=nth, seconds=dt,
-                sample=f"prefill CSM round (s={n}, c={w.c}, m={m}) of {BH} (layer, KV head) units "
-                       f"= {layers} layers x {w.h_kv} heads of the {w.layers}-layer stack, fp64 oracle")
+    res = dict(value=tokens / dt, unit="tokens/s", cores=nth, seconds=dt,
+               sample=f"prefill CSM round (s={n}, c={w.c}, m={m}) of {BH} (layer, KV head) units "
+                      f"= {layers} layers x {w.h_kv} heads of the {w.layers}-layer stack, fp64 oracle")
+    if decode:
+        # one decode step's log-N attention over the compressed sample (the first layer's
+        # heads, G query heads each), in the same algorithmic bytes as the GPU metric
+        h = w.h_kv
+        Kc = out["K"][:h].reshape(1, h, cap, ws.d)
+        Vc = out["V"][:h].reshape(1, h, cap, ws.d)
+        Nc = out["N"][:h].reshape(1, h, cap)
+        Lc = out["len"][:h].reshape(1, h)
+        q = np.random.default_rng(0).standard_normal((1, w.h_q, ws.d))
+        t0 = time.perf_counter()
+        oracle.decode_attn_logn(q, Kc, Vc, Nc, Lc, w.h_q, nthreads=nth)
+        da = time.perf_counter() - t0
+        nbytes = int(Lc.sum()) * row_bytes(w) + w.h_q * ws.d * (2 if w.dtype == "bf16" else 4) * 2
+        res["decode"] = {"value": nbytes / da / 1e9, "unit": "GB/s", "seconds": da,
+                         "sample": f"one decode step of log-N attention over {h} compressed KV heads "
+                                   f"({int(Lc[0, 0])} tokens each), {w.h_q} query heads, fp64 oracle"}
+    return res
 
 
 def dist_setup(n_gpus):
@@ -394,7 +411,7 @@ def run_gpu(args):
     per_launch_bytes = attn_bytes_step / w.steps
     avg_launch_s = (attn_ms / 1e3) / max(1, attn_calls)
     csm_gbs = csm_bytes_step * args.steps / (csm_ms / 1e3) / 1e9
-    cpu = oracle_sample(w, units=args.cpu_units) if not args.no_cpu_baseline else None
+    cpu = oracle_sample(w, units=args.cpu_units, decode=True) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC,
         "value": agg["tokens"] / agg["csm_s"],
@@ -436,7 +453,7 @@ def run_gpu(args):
     }
     if cpu is not None:
         line["cpu_baseline"] = {"value": cpu["value"], "unit": "tokens/s", "cores": cpu["cores"], "kind": "oracle",
-                                "sample": cpu["sample"], "seconds": cpu["seconds"]}
+                                "sample": cpu["sample"], "seconds": cpu["seconds"], "decode": cpu.get("decode")}
     print(json.dumps(line))
     return 0
 
