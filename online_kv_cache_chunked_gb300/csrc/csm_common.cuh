@@ -1,5 +1,5 @@
 // csm_common.cuh -- parts of one Chunked Soft Matching round shared by the
-// tensor-core kernel (csm_tc.cu) and the CUDA-core kernel (csm_compress.cu):
+// tensor-core kernels (csm_tc3.cu, csm_tc.cu) and the CUDA-core kernel (csm_compress.cu):
 // work-item bookkeeping, the top-m selection and compaction tables, the
 // degree-weighted merge of output rows and the tail move.
 // [Chelsea §三 分块软匹配算法 steps 1-4; CentroidKV 分块软匹配 (CSM), 聚合]

@@ -1,7 +1,7 @@
 // csm_compress.cu -- one Chunked Soft Matching round on every (sequence, KV head)
-// of a cache, compacted in place: the C entry points, the per-call prologue and
-// the CUDA-core kernel (fp32 caches and shapes the tensor-core kernel in
-// csm_tc.cu does not cover). [Chelsea §三 分块软匹配算法 steps 1-4;
+// of a cache, compacted in place: the C entry points, the per-call prologue,
+// the choice of kernel, and the CUDA-core kernel (fp32 caches and the shapes the
+// tensor-core kernels in csm_tc3.cu, the default, and csm_tc.cu do not cover). [Chelsea §三 分块软匹配算法 steps 1-4;
 // CentroidKV 分块软匹配 (CSM), 聚合]
 //
 // Work decomposition

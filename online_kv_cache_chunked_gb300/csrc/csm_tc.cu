@@ -1,5 +1,7 @@
 // csm_tc.cu -- Chunked Soft Matching on the tensor cores (bf16, c = 256,
-// d in {64, 128}). [Chelsea §三 分块软匹配算法 steps 1-4; CentroidKV 分块软匹配 (CSM), 聚合]
+// d in {64, 128}), one 16-warp CTA per SM with a slot ring: the alternative to
+// the three-CTAs-per-SM kernel in csm_tc3.cu (the default), selected with
+// CSM_KERNEL_TC_RING. [Chelsea §三 分块软匹配算法 steps 1-4; CentroidKV 分块软匹配 (CSM), 聚合]
 //
 // One persistent CTA per SM walks work tickets (level-major: chunk j of every
 // unit, then the tail pieces) through a ring of three 64 KB shared-memory slots
