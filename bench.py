@@ -39,7 +39,7 @@ METRIC = "CSM KV tokens compressed/s; log-N decode-attn HBM GB/s (% of peak), 1Ã
 FALLBACK_HBM_GBS = 6800.0
 
 
-CSM_KERNELS = {"auto": 0, "simt": 1, "ring": 2, "split": 3}
+CSM_KERNELS = {"auto": 0, "simt": 1, "split": 3}
 L2_BYTES = 128 << 20  # GB300 L2 is about 129 MB
 
 
@@ -572,7 +572,7 @@ def main():
     ap.add_argument("--budget-exact", action="store_true",
                     help="each round merges only the oldest chunks needed to bring s under the budget")
     ap.add_argument("--csm-kernel", default="auto", choices=sorted(CSM_KERNELS),
-                    help="compression kernel: auto, simt (CUDA cores), ring or split (tensor cores)")
+                    help="compression kernel: auto, simt (CUDA cores) or split (tensor cores)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -138,7 +138,7 @@ typedef struct {
  * the order of fp32 rounding in the similarity scores. */
 #define CSM_KERNEL_AUTO 0
 #define CSM_KERNEL_SIMT 1    /* fp32 CUDA cores, one persistent CTA per SM */
-#define CSM_KERNEL_TC_RING 2 /* tcgen05, one CTA per SM with a 3-slot TMA ring */
+/* (value 2 is not used: any value other than those listed is CSMKV_ERR_ARG) */
 #define CSM_KERNEL_TC_SPLIT 3 /* tcgen05, three CTAs per SM with one slot each */
 
 /* csm_compress plus two optional outputs/controls:

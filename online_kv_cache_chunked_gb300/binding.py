@@ -38,7 +38,7 @@ class CsmOptions(ctypes.Structure):
                 ("kernel", ctypes.c_int32), ("seq_max_chunks", ctypes.c_void_p)]
 
 
-CSM_KERNEL_AUTO, CSM_KERNEL_SIMT, CSM_KERNEL_TC_RING, CSM_KERNEL_TC_SPLIT = 0, 1, 2, 3
+CSM_KERNEL_AUTO, CSM_KERNEL_SIMT, CSM_KERNEL_TC_SPLIT = 0, 1, 3
 
 
 class CsmRoundPlan(ctypes.Structure):

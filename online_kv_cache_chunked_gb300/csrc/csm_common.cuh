@@ -1,5 +1,5 @@
 // csm_common.cuh -- parts of one Chunked Soft Matching round shared by the
-// tensor-core kernels (csm_tc3.cu, csm_tc.cu) and the CUDA-core kernel (csm_compress.cu):
+// tensor-core kernel (csm_tc3.cu) and the CUDA-core kernel (csm_compress.cu):
 // work-item bookkeeping, the top-m selection and compaction tables, the
 // degree-weighted merge of output rows and the tail move.
 // [Chelsea §三 分块软匹配算法 steps 1-4; CentroidKV 分块软匹配 (CSM), 聚合]
@@ -342,9 +342,7 @@ __device__ bool tail_piece(const CsmParams& p, int u, int piece, int32_t epoch, 
     return true;
 }
 
-// Tensor-core launchers: one persistent CTA per SM with a TMA ring (csm_tc.cu),
-// three CTAs per SM with one slot each (csm_tc3.cu).
+// Tensor-core launcher: three CTAs per SM with one slot each (csm_tc3.cu).
 int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st);
-int launch_csm_tc(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st);
 
 }  // namespace csmkv

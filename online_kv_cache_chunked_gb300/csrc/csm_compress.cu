@@ -1,7 +1,7 @@
 // csm_compress.cu -- one Chunked Soft Matching round on every (sequence, KV head)
 // of a cache, compacted in place: the C entry points, the per-call prologue,
 // the choice of kernel, and the CUDA-core kernel (fp32 caches and the shapes the
-// tensor-core kernels in csm_tc3.cu, the default, and csm_tc.cu do not cover). [Chelsea §三 分块软匹配算法 steps 1-4;
+// tensor-core kernel in csm_tc3.cu, the default, does not cover). [Chelsea §三 分块软匹配算法 steps 1-4;
 // CentroidKV 分块软匹配 (CSM), 聚合]
 //
 // Work decomposition
@@ -252,6 +252,8 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     int32_t L;
     const size_t need = csm_layout(cache, n1, n2, c, &o_snap, &o_ch, &o_tp, &o_fkn, &o_fv, &L);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
+    const int want = opts ? opts->kernel : CSM_KERNEL_AUTO;
+    if (want != CSM_KERNEL_AUTO && want != CSM_KERNEL_SIMT && want != CSM_KERNEL_TC_SPLIT) return CSMKV_ERR_ARG;
     const int32_t maxch = csm_max_chunks(cache, n1, n2, c);
     if (m == 0 || maxch == 0) return CSMKV_OK;  // nothing can merge
 
@@ -289,11 +291,8 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;
 
     const int D = cache->head_dim;
-    const int want = opts ? opts->kernel : CSM_KERNEL_AUTO;
-    if (want < CSM_KERNEL_AUTO || want > CSM_KERNEL_TC_SPLIT) return CSMKV_ERR_ARG;
     const bool tc = cache->dtype == CSMKV_BF16 && c == 256 && (D == 64 || D == 128) && want != CSM_KERNEL_SIMT;
     const uint64_t rows = (uint64_t)cache->batch * cache->h_kv * cache->cap;
-    if (tc && want == CSM_KERNEL_TC_RING) return launch_csm_tc(P, D, K, V, N, rows, st);
     if (tc) return launch_csm_tc3(P, D, K, V, N, rows, st);
     const int RB = D * (int)dtype_bytes(cache->dtype);
     const int smem = csm_stage_bytes_simt(c, RB) + (int)sizeof(CsmTables) + 257 * 4 + 1024;

@@ -808,11 +808,10 @@ extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t 
     return dec_layout(cache, nCTA, &a, &b, &c, &d, &e, &f);
 }
 
-// Attention over the cache, optionally with the step's new token appended first
-// (k_new != NULL: bf16 fuses the append into the attention kernel).
-static int decode_attn_impl(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
-                            const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
-                            void* out, void* workspace, size_t ws_bytes, void* stream) {
+namespace csmkv {
+int decode_attn_check_args(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                           const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
+                           const void* out) {
     int rc = check_cache(cache);
     if (rc != CSMKV_OK) return rc;
     if (!q || !K || !V || !N || !len || !out) return CSMKV_ERR_ARG;
@@ -825,8 +824,21 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
         return CSMKV_ERR_ALIGN;
     const int G = h_q / cache->h_kv;
     const int D = cache->head_dim;
+    if (cache->dtype == CSMKV_BF16 && (G > 8 || (D != 64 && D != 128))) return CSMKV_ERR_UNSUPPORTED;
+    return CSMKV_OK;
+}
+}  // namespace csmkv
+
+// Attention over the cache, optionally with the step's new token appended first
+// (k_new != NULL: bf16 fuses the append into the attention kernel).
+static int decode_attn_impl(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                            const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
+                            void* out, void* workspace, size_t ws_bytes, void* stream) {
+    int rc = decode_attn_check_args(q, K, V, N, len, k_new, v_new, cache, h_q, scale, out);
+    if (rc != CSMKV_OK) return rc;
+    const int G = h_q / cache->h_kv;
+    const int D = cache->head_dim;
     const bool bf16 = cache->dtype == CSMKV_BF16;
-    if (bf16 && (G > 8 || (D != 64 && D != 128))) return CSMKV_ERR_UNSUPPORTED;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return CSMKV_ERR_CUDA;
     size_t o_prefix, o_cta, o_cnt, o_pm, o_pl, o_pacc;

@@ -46,9 +46,10 @@ int scratch_for_current_device(void** out) {
 extern "C" int decode_attn_logn_noalloc(const void* q, const void* K, const void* V, const int32_t* N,
                                         const int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale,
                                         void* out, void* stream) {
-    int rc = csmkv::check_cache(cache);
+    // Every argument check runs before the shared array is touched, so a rejected
+    // call leaves it (and any call still running on it) alone.
+    int rc = csmkv::decode_attn_check_args(q, K, V, N, len, nullptr, nullptr, cache, h_q, scale, out);
     if (rc != CSMKV_OK) return rc;
-    if (h_q < 1 || (h_q % cache->h_kv) != 0) return CSMKV_ERR_ARG;
     const size_t need = decode_attn_workspace_bytes(cache, h_q);
     if (need == 0) return CSMKV_ERR_CUDA;
     if (need > kNoAllocScratchBytes) return CSMKV_ERR_WORKSPACE;  // batch too large for the fixed scratch

@@ -72,6 +72,12 @@ int sm_count();                 // SMs of the current device (cached per device)
 int set_kernel_smem(const void* fn, int bytes, bool max_carveout = false);
 const void* encode_fn();        // cuTensorMapEncodeTiled, or nullptr
 
+// Argument checks of decode attention (everything but the workspace): the
+// status decode_attn_logn / decode_step_logn would return before launching.
+int decode_attn_check_args(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                           const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
+                           const void* out);
+
 // Encodes a tiled tensor map; returns false on failure.
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box,

@@ -182,14 +182,20 @@ class Pipeline:
         """(step, r, seq_mask, seq_max_chunks) of every round after prefill, in issue order."""
         return [(rd.step, rd.r, self.masks[k], self.limits[k]) for k, rd in enumerate(self.rounds) if rd.step >= 1]
 
+    def decode_native(self, first_step, steps, attn_events=None, csm_events=None, l2_flush=None, fused=True):
+        """Decode steps first_step .. first_step + steps - 1 issued by the library in one
+        call, with the rounds the plan fires at those steps (fused: each step's append
+        and attention as one kernel)."""
+        d, w = self.d, self.w
+        B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], d["q"], d["k_dec"], d["v_dec"], self.out, w.n1, w.n2,
+                         w.c, rounds=self.decode_plan(), head_mask=self.head_mask, ws_csm=self.ws_csm,
+                         ws_append=self.ws_app, ws_attn=self.ws_att, first_step=first_step, steps=steps,
+                         csm_kernel=self.csm_kernel, attn_events=attn_events, csm_events=csm_events,
+                         l2_flush=l2_flush, stream=self.stream, fused_append=fused)
+
     def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None, fused=True):
         """Prefill round(s), then the whole decode loop issued by the library in one call
         (fused: each step's append and attention as one kernel)."""
-        d, w = self.d, self.w
         self.compress_at(0, hook)
-        n = w.steps if steps is None else steps
-        B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], d["q"], d["k_dec"], d["v_dec"], self.out, w.n1, w.n2,
-                         w.c, rounds=self.decode_plan(), head_mask=self.head_mask, ws_csm=self.ws_csm,
-                         ws_append=self.ws_app, ws_attn=self.ws_att, first_step=1, steps=n,
-                         csm_kernel=self.csm_kernel, attn_events=attn_events, csm_events=csm_events,
-                         l2_flush=l2_flush, stream=self.stream, fused_append=fused)
+        n = self.w.steps if steps is None else steps
+        self.decode_native(1, n, attn_events, csm_events, l2_flush, fused)

@@ -14,10 +14,21 @@ match that replay: lengths and degrees exactly, rows that are plain copies
 bit-exactly, merged centroids within the value tolerance.
 
 Value tolerance for merged K/V rows (per (sequence, head) unit, range = max - min
-of the oracle's rows): bf16 storage 1e-3 * range + one bf16 ulp of the oracle
-value (rounding to bf16 alone can exceed 1e-3 * range); fp32 storage
-1e-6 * range + 4 fp32 ulps. Attention outputs: 2e-2 absolute for bf16, 1e-5
-for fp32.
+of the oracle's rows, amax = max |x| of the rows merged from). bf16 storage:
+
+    1e-3 * range + 1/2 bf16 ulp(oracle value) + 2^-16 * amax.
+
+The device forms sum_i n_i x_i with k <= c/2 + 1 fp32 fused multiply-adds,
+multiplies by fl(1 / sum n_i) and rounds once to bf16. The fp32 part is off
+the exact mean y by at most (k + 2) 2^-24 sum n_i |x_i| / sum n_i
+<= 131 * 2^-24 amax < 2^-16 amax (c <= 256); rounding that to bf16 adds at
+most half a bf16 ulp of y (if the fp32 value crosses a power of two the bf16
+result is that power, no farther from y than the fp32 value). 1e-3 * range is
+the stated bound on top. fp32 storage: 1e-6 * range + 4 fp32 ulps.
+Attention outputs: 2e-2 absolute for bf16, 1e-5 for fp32.
+
+Near-ties: check_round can collect one record per deviating decision (unit,
+chunk, A index, device and oracle choices, the oracle's margin) for logging.
 """
 from __future__ import annotations
 
@@ -35,10 +46,14 @@ def ulp(x, dtype):
     return np.exp2(e - mant)
 
 
-def value_tol(ref_rows, dtype):
+def value_tol(ref_rows, dtype, src_rows=None):
+    """Per-element bound for merged rows; src_rows: the pre-round rows they are merged
+    from (default: ref_rows), for the fp32 summation term."""
     rng = float(ref_rows.max() - ref_rows.min()) if ref_rows.size else 0.0
     if dtype == "bf16":
-        return 1e-3 * rng + ulp(ref_rows, dtype)
+        src = ref_rows if src_rows is None else src_rows
+        amax = float(np.abs(src).max()) if np.size(src) else 0.0
+        return 1e-3 * rng + 0.5 * ulp(ref_rows, dtype) + 2.0 ** -16 * amax
     return 1e-6 * rng + 4 * ulp(ref_rows, dtype)
 
 
@@ -70,9 +85,28 @@ def check_chunk_decisions(Kc, free_match, free_sim, gpu_match, m, tol=NEAR_TIE):
     return True, None
 
 
-def check_round(pre_K, free, gpu_match, n_chunks, m, n1, c, units=None):
+def deviation_records(free_match, free_sim, free_margin, free_cut, gpu_match):
+    """One record per A token whose device decision differs from the oracle's:
+    a, device and oracle targets (-1 = not selected), and the oracle margin that
+    decided it -- the argmax margin (best minus second-best cosine) when the
+    target differs, the chunk's top-m cut margin (m-th minus (m+1)-th largest
+    edge similarity) when only its selection differs."""
+    out = []
+    g = np.asarray(gpu_match)
+    for a in np.nonzero(g != free_match)[0]:
+        gb, fb = int(g[a]), int(free_match[a])
+        if gb >= 0 and fb >= 0:
+            kind, margin = "argmax", float(free_margin[a])
+        else:
+            kind, margin = "cut", float(free_cut)
+        out.append(dict(a=int(a), device=gb, oracle=fb, kind=kind, oracle_margin=margin))
+    return out
+
+
+def check_round(pre_K, free, gpu_match, n_chunks, m, n1, c, units=None, log=None):
     """Decision check for a full round. pre_K [BH, cap, d] fp64; free: oracle.csm_round
     output; gpu_match [BH, maxch, c/2]; n_chunks [BH] processed chunks per unit.
+    log: optional list; one record per deviating decision is appended to it.
     Returns (deviating chunk count, list of failures)."""
     dev, fails = 0, []
     units = range(pre_K.shape[0]) if units is None else units
@@ -84,6 +118,10 @@ def check_round(pre_K, free, gpu_match, n_chunks, m, n1, c, units=None):
             dev += int(d_)
             if f_:
                 fails.append(f"unit {u} chunk {j}: {f_}")
+            if d_ and log is not None:
+                for r in deviation_records(free["match"][u, j], free["sim"][u, j], free["margin"][u, j],
+                                           free["cut"][u, j], gpu_match[u, j]):
+                    log.append(dict(unit=int(u), chunk=int(j), **r))
     return dev, fails
 
 
@@ -108,7 +146,7 @@ def compare_state(replay, pre, gpu, dtype, units=None):
             if not np.array_equal(g[copies], pre[name][u, org[copies]]):
                 fails.append(f"unit {u}: {name} copied rows are not bit-exact")
             if mrg.any():
-                tol = value_tol(r, dtype)[mrg]
+                tol = value_tol(r, dtype, pre[name][u, :int(pre["len"][u])])[mrg]
                 err = np.abs(g[mrg] - r[mrg])
                 worst = max(worst, float((err / tol).max()))
                 if np.any(err > tol):

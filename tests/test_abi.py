@@ -114,6 +114,10 @@ def test_csm_argument_errors_without_gpu(lib):
     assert _compress(lib, c, ptr=4100) == 3               # misaligned
     assert _compress(lib, c, ws=16) == 5                  # workspace too small
     assert _compress(lib, c, wsp=4096 + 16) == 5          # workspace misaligned
+    opts = B.CsmOptions(kernel=2)  # not a kernel choice
+    P = ctypes.c_void_p
+    assert lib.csm_compress_ex(P(4096), P(4096), P(4096), P(4096), ctypes.byref(c), 16, 64, 256, 0.5, None, None,
+                               None, ctypes.byref(opts), P(1 << 16), 1 << 20, None) == 1
     need = lib.csm_workspace_bytes(ctypes.byref(c), 16, 64, 256)
     assert need > 256
     assert lib.csm_max_chunks(ctypes.byref(c), 16, 64, 256) == (1024 - 80) // 256
@@ -133,6 +137,23 @@ def test_attention_argument_errors_without_gpu(lib):
     assert call(h_q=18) == 8         # bf16 group of 9 query heads is not covered
     assert call(cache=_cache(head_dim=96)) == 8
     assert lib.csm_append(None, None, None, None, ctypes.byref(c), None, None, None, None, 0, None) == 1
+
+
+def test_no_workspace_attention_checks_arguments_before_touching_the_gpu(lib):
+    """The no-workspace entry point runs every argument check before it looks up or
+    clears its shared scratch, so these return at once here, with no GPU at all."""
+    P = ctypes.c_void_p
+    c = _cache()
+
+    def call(h_q=8, scale=0.088, ptr=4096, cache=c, q=4096):
+        return lib.decode_attn_logn_noalloc(P(q), P(ptr), P(ptr), P(ptr), P(ptr), ctypes.byref(cache), h_q,
+                                            scale, P(ptr), None)
+    assert call(h_q=3) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(q=0) == 1            # NULL query
+    assert call(ptr=4104) == 3
+    assert call(h_q=18) == 8
+    assert call(cache=_cache(dtype=9)) == 2
 
 
 def test_decode_run_rejects_bad_arguments_without_a_gpu(lib):

@@ -6,6 +6,7 @@ import torch
 import oracle
 from online_kv_cache_chunked_gb300 import synth
 from online_kv_cache_chunked_gb300.pipeline import Pipeline, final_lengths
+from online_kv_cache_chunked_gb300 import binding as B
 from tests.gpu_helpers import attn_parity, to64
 
 pytestmark = pytest.mark.gpu
@@ -62,6 +63,69 @@ def test_ragged_batch_pipeline_lengths(cuda_lib):
     b = 5
     attn_parity(d["q"][-1][b:b + 1], d["K"][b:b + 1], d["V"][b:b + 1], d["N"][b:b + 1], d["len"][b:b + 1],
                 p.out[-1][b:b + 1], "bf16")
+
+
+def _attention_at_steps_against_oracle(w, d, checks):
+    """Runs the workload in the configuration the benchmark times (prefill rounds,
+    then the natively issued loop of fused append + attention steps with the planned
+    rounds) and, at every step i in `checks`, compares all query heads' outputs with
+    the oracle: the cache as it stood before step i, plus that step's appended token,
+    through oracle.append and oracle.decode_attn_logn. Returns the errors."""
+    p = Pipeline(w, d)
+    p.compress_at(0)
+    done, errs = 0, {}
+    for i in sorted(checks):
+        if i - 1 > done:
+            p.decode_native(done + 1, i - 1 - done)
+        torch.cuda.synchronize()
+        L = d["len"].cpu().numpy()
+        top = int(L.max()) + 1
+        BH = w.batch * w.h_kv
+        pre = [to64(d["K"][:, :, :top]).reshape(BH, top, w.d), to64(d["V"][:, :, :top]).reshape(BH, top, w.d),
+               d["N"][:, :, :top].cpu().numpy().reshape(BH, top), L.reshape(BH)]
+        p.decode_native(i, 1)
+        done = i
+        torch.cuda.synchronize()
+        K, V, N, Ln, full = oracle.append(*pre, to64(d["k_dec"][i - 1]).reshape(BH, w.d),
+                                          to64(d["v_dec"][i - 1]).reshape(BH, w.d))
+        assert full == 0
+        ref = oracle.decode_attn_logn(to64(d["q"][i - 1]), K.reshape(w.batch, w.h_kv, top, w.d),
+                                      V.reshape(w.batch, w.h_kv, top, w.d), N.reshape(w.batch, w.h_kv, top),
+                                      Ln.reshape(w.batch, w.h_kv), w.h_q)
+        got = to64(p.out[i - 1])
+        assert np.isfinite(got).all()
+        errs[i] = float(np.abs(got - ref).max())
+        assert errs[i] <= 2e-2, (i, errs[i])
+    if done < w.steps:
+        p.decode_native(done + 1, w.steps - done)
+    torch.cuda.synchronize()
+    for ws in (p.ws_csm, p.ws_app, p.ws_att):
+        assert B.csmkv_device_status(ws) == 0
+    assert np.array_equal(d["len"].cpu().numpy(), final_lengths(w))
+    return errs
+
+
+def test_32k_batch4_attention_against_oracle(cuda_lib):
+    """The 32K x batch-4 workload at full size: three progressive rounds (m = 128, 115,
+    102) on 7 of 8 KV heads, the outlier head left at ~33K tokens, then 1000 fused decode
+    steps; every query head checked against the oracle at steps 1, 2, 3, 100 and 1000
+    (steps 1 and 2 also fire rounds after their attention)."""
+    w = synth.WORKLOADS["llama_32k_b4"]
+    d = synth.make_device(w)
+    hm = d["head_mask"].cpu().numpy()
+    assert hm.sum() == 1
+    errs = _attention_at_steps_against_oracle(w, d, {1, 2, 3, 100, w.steps})
+    L = d["len"].cpu().numpy()
+    assert np.all(L[:, hm == 1] == 32768 + w.steps) and np.all(L[:, hm == 0] == 5584 + w.steps - 2)
+    print("32k x4 attention errors at sampled steps:", errs)
+
+
+def test_ragged_batch_attention_against_oracle(cuda_lib):
+    """The ragged 16-sequence batch at full size, every query head at steps 1, 2, 3, 256
+    and 512 (the last)."""
+    w = synth.WORKLOADS["qwen2_ragged"]
+    d = synth.make_device(w)
+    print("ragged attention errors:", _attention_at_steps_against_oracle(w, d, {1, 2, 3, 256, w.steps}))
 
 
 @pytest.mark.parametrize("name,steps", [("llama_32k_b4", 12), ("qwen2_ragged", 40)])
