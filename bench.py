@@ -57,9 +57,12 @@ def row_bytes(w):
 
 
 def csm_call_stats(w, rd, head_mask):
-    """Tokens and algorithmic bytes of one CSM call (per the round's sequences)."""
+    """Tokens and algorithmic bytes of one CSM call (per the round's sequences). A
+    token is one row of one layer's cache (all its KV heads), so a shard that holds
+    some of the KV heads counts that fraction of each token."""
     rb = row_bytes(w)
     active_heads = w.h_kv - int(np.asarray(head_mask).sum())
+    head_frac = w.h_kv / w.global_shape[2]
     tokens = 0
     nbytes = 0
     for k, s in enumerate(rd.s_before):
@@ -68,7 +71,7 @@ def csm_call_stats(w, rd, head_mask):
         if rd.limits and rd.limits[k] > 0:  # budget-exact round: only the oldest chunks
             ch = min(ch, rd.limits[k])
         tail = s - (w.n1 + ch * w.c) if ch else 0
-        tokens += s * w.layers
+        tokens += s * w.layers * head_frac
         per_head = ch * w.c * rb + ch * (w.c - rd.m) * rb + 2 * tail * rb
         nbytes += per_head * active_heads * w.layers
     return tokens, nbytes
@@ -170,7 +173,8 @@ def oracle_sample(w, units=16, threads=None, decode=False):
     from online_kv_cache_chunked_gb300 import synth
 
     layers = max(1, units // w.h_kv)
-    ws = synth.scaled(w, layers=layers, seqs=1, n=(w.n[0],), steps=1, name=w.name + "_sample")
+    ws = synth.scaled(w, layers=layers, seqs=1, n=(w.n[0],), steps=1, name=w.name + "_sample", layer0=0, seq0=0,
+                      head0=0, layers_total=0, seqs_total=0, h_kv_total=0)
     data = synth.make_numpy(ws)
     BH = ws.batch * ws.h_kv
     n = ws.n[0]
@@ -284,14 +288,26 @@ def workload_of(args):
     return synth.scaled(w, budget_exact=True) if getattr(args, "budget_exact", False) else w
 
 
-def config_of(w):
+def config_of(w, world=1):
+    L, S, H = w.global_shape
+    par = "1 GPU"
+    if world > 1:
+        par = (f"{world} ranks, one GPU each; (layer, sequence, KV head) units sharded by "
+               f"{synth_axis(w)} (per rank: {w.layers} layers x {w.seqs} sequences x {w.h_kv} KV heads); "
+               "no collective on the data path")
     return {"workload": w.name, "layers": w.layers, "sequences": w.seqs, "kv_heads": w.h_kv, "q_heads": w.h_q,
             "head_dim": w.d, "prefill_tokens": list(w.n) if len(set(w.n)) > 1 else w.n[0],
             "decode_steps": w.steps, "cache_dtype": w.dtype, "n1": w.n1, "n2": w.n2, "c": w.c, "R": w.R,
             "r_init": w.r_init, "delta_r": w.dr, "r_min": w.r_min, "g": w.g, "outlier_frac": w.outlier_frac,
             "budget_exact": w.budget_exact,
-            "parallelism": "independent replicas per GPU (no collective)",
+            "whole_job": {"layers": L, "sequences": S, "kv_heads": H},
+            "parallelism": par,
             "l2": "inputs larger than L2: each decode step reads ~1.1 GB of cache, each prefill round ~13 GB"}
+
+
+def synth_axis(w):
+    from online_kv_cache_chunked_gb300 import synth
+    return synth.shard_axis(w)
 
 
 def run_gpu(args):
@@ -307,7 +323,8 @@ def run_gpu(args):
     if not os.path.exists(_build.OUT):
         _build.build()
     B.load()
-    w = workload_of(args)
+    # each rank runs its own shard of the job's units (no exchange between ranks)
+    w = synth.shard(workload_of(args), rank, world, args.shard)
     stream = torch.cuda.current_stream()
     d = synth.make_device(w)
     K0, V0, N0, L0 = (d[k].clone() for k in ("K", "V", "N", "len"))
@@ -421,11 +438,11 @@ def run_gpu(args):
         "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if (world > 1 and args.shard == "strong") else "weak",
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded AR(1) keys, N(0,1) values, N(0,I) queries; no model weights)",
-        "config": dict(config_of(w), l2=("a 2xL2 buffer is read before every attention call" if flush is not None
+        "config": dict(config_of(w, world), l2=("a 2xL2 buffer is read before every attention call" if flush is not None
                                           else "every attention call reads more than 2xL2 of cache"),
                        csm_kernel=args.csm_kernel),
         "decode_attn": {"value": attn_gbs, "unit": "GB/s", "frac_of_measured_peak": attn_gbs / hbm,
@@ -571,6 +588,9 @@ def main():
                     help="zero a 2xL2 buffer before every attention call (auto: when a call reads < 2xL2)")
     ap.add_argument("--budget-exact", action="store_true",
                     help="each round merges only the oldest chunks needed to bring s under the budget")
+    ap.add_argument("--shard", default="weak", choices=["weak", "strong"],
+                    help="with N ranks: weak = N copies of the workload's shape, one per rank (per-GPU work "
+                         "fixed); strong = the workload's own units split over the ranks")
     ap.add_argument("--csm-kernel", default="auto", choices=sorted(CSM_KERNELS),
                     help="compression kernel: auto, simt (CUDA cores) or split (tensor cores)")
     args = ap.parse_args()

@@ -52,6 +52,25 @@ class Workload:
     seed: int
     forced_round: bool = False  # run one round regardless of the trigger (the tiny case)
     budget_exact: bool = False  # each round merges only the oldest chunks needed to reach B
+    # A shard of a larger workload (see shard()): this workload holds layers
+    # [layer0, layer0 + layers), sequences [seq0, seq0 + seqs) and KV heads
+    # [head0, head0 + h_kv) of one with layers_total x seqs_total x h_kv_total
+    # (0 = the same as the shard's own count).
+    layer0: int = 0
+    seq0: int = 0
+    head0: int = 0
+    layers_total: int = 0
+    seqs_total: int = 0
+    h_kv_total: int = 0
+
+    @property
+    def global_shape(self):
+        """(layers, sequences, KV heads) of the whole workload this one is part of."""
+        return (self.layers_total or self.layers, self.seqs_total or self.seqs, self.h_kv_total or self.h_kv)
+
+    @property
+    def is_shard(self) -> bool:
+        return self.global_shape != (self.layers, self.seqs, self.h_kv)
 
     @property
     def batch(self) -> int:
@@ -98,16 +117,19 @@ def scaled(w: Workload, **kw) -> Workload:
 
 def head_stats(w: Workload):
     """Per (layer, KV head) rho [layers, h_kv] and mean offset mu [layers, h_kv, d] (float64),
-    and the outlier-head mask [h_kv] (uint8), all from the workload seed."""
+    and the outlier-head mask [h_kv] (uint8), all from the workload seed. A shard gets
+    its rows of the whole workload's statistics."""
+    Lt, _, Ht = w.global_shape
     rng = np.random.default_rng(w.seed)
     lo, hi = w.rho
-    rho = rng.uniform(lo, hi, (w.layers, w.h_kv)) if hi > lo else np.full((w.layers, w.h_kv), lo)
-    mu = rng.normal(0.0, w.mu_std, (w.layers, w.h_kv, w.d)) if w.mu_std > 0 else np.zeros((w.layers, w.h_kv, w.d))
-    mask = np.zeros(w.h_kv, np.uint8)
+    rho = rng.uniform(lo, hi, (Lt, Ht)) if hi > lo else np.full((Lt, Ht), lo)
+    mu = rng.normal(0.0, w.mu_std, (Lt, Ht, w.d)) if w.mu_std > 0 else np.zeros((Lt, Ht, w.d))
+    mask = np.zeros(Ht, np.uint8)
     if w.outlier_frac > 0:
-        k = max(1, int(round(w.outlier_frac * w.h_kv)))
-        mask[rng.choice(w.h_kv, size=k, replace=False)] = 1
-    return rho, mu, mask
+        k = max(1, int(round(w.outlier_frac * Ht)))
+        mask[rng.choice(Ht, size=k, replace=False)] = 1
+    ls, hs = slice(w.layer0, w.layer0 + w.layers), slice(w.head0, w.head0 + w.h_kv)
+    return rho[ls, hs], mu[ls, hs], mask[hs]
 
 
 def make_numpy(w: Workload):
@@ -116,6 +138,7 @@ def make_numpy(w: Workload):
     Returns dict with K, V: [batch, h_kv, n_max + steps, d] (keys of prefill and decode
     positions), q: [steps, batch, h_q, d], lengths [seqs], rho, mu, head_mask.
     """
+    assert not w.is_shard, "make_numpy serves whole workloads; shards use make_device"
     rho, mu, mask = head_stats(w)
     rng = np.random.default_rng(w.seed + 1)
     B, H, d = w.batch, w.h_kv, w.d
@@ -160,40 +183,53 @@ def _ar1_device(rho_u: torch.Tensor, T: int, d: int, gen: torch.Generator, block
     return out[:, :T]
 
 
+def _group_seed(w: Workload, layer: int, seq: int) -> int:
+    """Seed of the inputs of one (layer, sequence) of the whole workload."""
+    return (w.seed * 1_000_003 + 7919 * layer + seq + 1) % (2 ** 63)
+
+
 def make_device(w: Workload, device="cuda"):
     """All inputs generated on the device in the cache dtype.
+
+    Every (layer, sequence) draws its inputs (all KV heads of the whole workload,
+    their decode keys and values, its query heads) from a generator seeded by its
+    global indices, so a shard of a workload (shard()) gets exactly the inputs
+    the whole workload has at its units.
 
     Returns dict with K, V: [batch, h_kv, cap, d] (prefill rows filled, N=1, len=n per
     sequence), k_dec, v_dec: [steps, batch, h_kv, d], q: [steps, batch, h_q, d],
     lengths [seqs] (host), head_mask (device uint8 [h_kv]).
     """
-    rho, mu, mask = head_stats(w)
-    gen = torch.Generator(device=device)
-    gen.manual_seed(w.seed + 1)
+    _, _, Ht = w.global_shape
+    G = w.h_q // w.h_kv
+    rho_all, mu_all, mask = _global_rows(w)
     B, H, d, cap = w.batch, w.h_kv, w.d, w.cap
-    T = max(w.n) + w.steps
     dt = w.torch_dtype
     K = torch.zeros((B, H, cap, d), dtype=dt, device=device)
     V = torch.zeros((B, H, cap, d), dtype=dt, device=device)
     k_dec = torch.empty((w.steps, B, H, d), dtype=dt, device=device)
     v_dec = torch.empty((w.steps, B, H, d), dtype=dt, device=device)
-    rho_u = torch.from_numpy(np.repeat(rho[:, None, :], w.seqs, axis=1).reshape(B * H)).to(device)
-    mu_u = torch.from_numpy(np.repeat(mu[:, None], w.seqs, axis=1).reshape(B * H, d)).to(device, torch.float32)
+    q = torch.empty((w.steps, B, w.h_q, d), dtype=dt, device=device)
     lengths = np.array(w.n, np.int64)
-    per = max(1, int(2 ** 31 // (T * d * 4 * 3)))  # units per chunk of the generator, bounded memory
-    for u0 in range(0, B * H, per):
-        u1 = min(B * H, u0 + per)
-        z = _ar1_device(rho_u[u0:u1], T, d, gen) + mu_u[u0:u1].view(-1, 1, d)
-        v = torch.randn((u1 - u0, T, d), generator=gen, device=device, dtype=torch.float32)
-        for u in range(u0, u1):
-            b, h = divmod(u, H)
-            n = int(lengths[b % w.seqs])
-            K[b, h, :n] = z[u - u0, :n].to(dt)
-            V[b, h, :n] = v[u - u0, :n].to(dt)
-            k_dec[:, b, h] = z[u - u0, n:n + w.steps].to(dt)
-            v_dec[:, b, h] = v[u - u0, n:n + w.steps].to(dt)
-        del z, v
-    q = torch.randn((w.steps, B, w.h_q, d), generator=gen, device=device, dtype=torch.float32).to(dt)
+    hs = slice(w.head0, w.head0 + H)
+    for l in range(w.layers):
+        rho_l = torch.from_numpy(rho_all[l]).to(device)                  # [Ht]
+        mu_l = torch.from_numpy(mu_all[l]).to(device, torch.float32)     # [Ht, d]
+        for sq in range(w.seqs):
+            b = l * w.seqs + sq
+            gen = torch.Generator(device=device)
+            gen.manual_seed(_group_seed(w, w.layer0 + l, w.seq0 + sq))
+            n = int(lengths[sq])
+            T = n + w.steps  # this sequence's prefill and decode positions
+            z = _ar1_device(rho_l, T, d, gen) + mu_l.view(Ht, 1, d)
+            v = torch.randn((Ht, T, d), generator=gen, device=device, dtype=torch.float32)
+            qg = torch.randn((w.steps, Ht * G, d), generator=gen, device=device, dtype=torch.float32)
+            K[b, :, :n] = z[hs, :n].to(dt)
+            V[b, :, :n] = v[hs, :n].to(dt)
+            k_dec[:, b] = z[hs, n:n + w.steps].transpose(0, 1).to(dt)
+            v_dec[:, b] = v[hs, n:n + w.steps].transpose(0, 1).to(dt)
+            q[:, b] = qg[:, w.head0 * G:(w.head0 + H) * G].to(dt)
+            del z, v, qg
     N = torch.zeros((B, H, cap), dtype=torch.int32, device=device)
     length = torch.zeros((B, H), dtype=torch.int32, device=device)
     for b in range(B):
@@ -202,6 +238,66 @@ def make_device(w: Workload, device="cuda"):
         length[b, :] = n
     return dict(K=K, V=V, N=N, len=length, k_dec=k_dec, v_dec=v_dec, q=q, lengths=lengths,
                 head_mask=torch.from_numpy(mask).to(device))
+
+
+def _global_rows(w: Workload):
+    """rho [layers, Ht] and mu [layers, Ht, d] over all KV heads of the whole workload
+    for this workload's layers, and this workload's outlier mask [h_kv]."""
+    whole_heads = dataclasses.replace(w, head0=0, h_kv=w.global_shape[2], h_q=w.h_q // w.h_kv * w.global_shape[2])
+    rho, mu, _ = head_stats(whole_heads)
+    _, _, mask = head_stats(w)
+    return rho, mu, mask
+
+
+def shard(w: Workload, rank: int, world: int, mode: str = "weak") -> Workload:
+    """Rank `rank`'s part when `world` ranks (one GPU each) run a workload.
+
+    The path has no exchange between (layer, sequence, KV head) units, so ranks
+    share nothing. "weak": the whole job is `world` copies of w's shape side by
+    side in the sequence dimension (sequences seqs * world), each rank running its
+    own seqs sequences with their own inputs -- per-GPU work stays fixed as ranks
+    are added. "strong": w's own units are split, by sequences, layers or KV heads
+    (the first of these that `world` divides), so the whole job stays fixed.
+    """
+    if world == 1:
+        return w
+    if not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside world {world}")
+    if w.is_shard:
+        raise ValueError("already a shard")
+    tag = f"{w.name}[{mode} {rank}/{world}]"
+    if mode == "weak":
+        return dataclasses.replace(w, seq0=rank * w.seqs, seqs_total=world * w.seqs, name=tag)
+    if mode != "strong":
+        raise ValueError(f"unknown shard mode {mode!r}")
+    if w.seqs % world == 0:
+        k = w.seqs // world
+        return dataclasses.replace(w, seq0=rank * k, seqs=k, seqs_total=w.seqs, n=tuple(w.n[rank * k:(rank + 1) * k]),
+                                   name=tag)
+    if w.layers % world == 0:
+        k = w.layers // world
+        return dataclasses.replace(w, layer0=rank * k, layers=k, layers_total=w.layers, name=tag)
+    if w.h_kv % world == 0:
+        k = w.h_kv // world
+        return dataclasses.replace(w, head0=rank * k, h_kv=k, h_q=w.h_q // world, h_kv_total=w.h_kv, name=tag)
+    raise ValueError(f"{w.name}: {world} ranks divide neither its sequences, layers nor KV heads")
+
+
+def shard_axis(w: Workload) -> str:
+    """Which dimension a shard cuts ("sequences", "layers", "kv heads" or "none")."""
+    L, S, H = w.global_shape
+    if S != w.seqs:
+        return "sequences"
+    if L != w.layers:
+        return "layers"
+    if H != w.h_kv:
+        return "kv heads"
+    return "none"
+
+
+def units(w: Workload):
+    """Global (layer, sequence, KV head) of every unit, in the cache's unit order."""
+    return [(w.layer0 + b // w.seqs, w.seq0 + b % w.seqs, w.head0 + h) for b in range(w.batch) for h in range(w.h_kv)]
 
 
 def cache_from_numpy(w: Workload, data, device="cuda"):
