@@ -182,9 +182,11 @@ int csm_append(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* ca
  * h_q must be a positive multiple of h_kv; bf16 needs G <= 8 and head_dim in
  * {64, 128} (CSMKV_ERR_UNSUPPORTED otherwise).
  * workspace: device, >= decode_attn_workspace_bytes(cache, h_q) bytes.
- * Work is split over the whole GPU by a flat partition of all units' tokens,
- * so ragged lengths stay balanced; partial softmax states are combined by a
- * second kernel.
+ * Work: every unit's rows are cut into fixed splits (boundaries depend only on
+ * the lengths) that a persistent grid takes from an atomic ticket, long units
+ * first, so ragged lengths and uneven SM bandwidth stay balanced; a second
+ * kernel merges each unit's per-split softmax states in split order. Results do
+ * not depend on which CTA ran which split (repeated calls are bit-identical).
  * ---------------------------------------------------------------------- */
 size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t h_q);
 
@@ -222,8 +224,9 @@ int decode_step_logn(const void* q, const void* k_new, const void* v_new, void* 
  * the workspace: the scratch is a fixed 16 MiB array inside the library, one
  * per GPU that loads it, held until the process exits.
  *  - Capacity: returns CSMKV_ERR_WORKSPACE when decode_attn_workspace_bytes(
- *    cache, h_q) exceeds 16 MiB (at head_dim 128 on 152 SMs: about 3700
- *    (sequence, KV head) units). Nothing is launched then.
+ *    cache, h_q) exceeds 16 MiB (at head_dim 128 on 152 SMs: about 5500
+ *    (sequence, KV head) units with 4 query heads per KV head, 1600 with 8).
+ *    Nothing is launched then.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
  *    stream capture.

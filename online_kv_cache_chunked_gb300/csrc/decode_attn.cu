@@ -5,19 +5,28 @@
 // online softmax keeps (m, l, acc) with p_t = n_t * 2^(x_t - m), x_t the
 // base-2 scaled logit. No log is evaluated and integer degrees stay exact.
 //
-// Work split (bf16): all units' tokens are laid end to end and cut into one
-// equal range per CTA, so ragged lengths (outlier heads, ragged batches) stay
-// balanced over the whole GPU. A CTA walks its range unit by unit in 64-token
-// tiles: one producer warp streams K, V (128-byte swizzled, 2 boxes of 64
-// columns) and the degree tile into a 3-stage TMA/mbarrier ring; four consumer
+// Work split (bf16). Every unit's tokens are cut into fixed splits: a base
+// length S (a multiple of the 64-token tile) chosen from the call's total so
+// that an equal share of the GPU is about kItemsPerCta splits, longer for long
+// units so no unit has more than kMaxSplitsPerUnit splits. The split boundaries
+// depend only on the lengths. A persistent grid (two CTAs per SM) takes splits
+// from one atomic ticket, units with many splits first, so the merges of the
+// long units' partial states happen early and the last wave is made of short
+// splits; SMs that stream faster simply take more splits. Inside a CTA one
+// producer warp claims the next split while the current one streams and feeds
+// K, V (128-byte swizzled, 2 boxes of 64 columns) and the degree tile into a
+// 3-stage TMA/mbarrier ring, tagging every stage with its split. Four consumer
 // warps each take 16 tokens of a tile and run S^T = K q^T and O^T += V^T P^T on
 // mma.sync (bf16 in, fp32 accumulate), the G <= 8 query heads of the group in
-// the N = 8 dimension, so each K/V byte is read once for the whole group. The
-// CTA merges its warps' states in shared memory and writes one partial
-// (m, l, acc) per unit it touched; the last CTA to
-// finish its part of a unit (a per-unit counter) merges the unit's partials into
-// the output. Unit offsets come from a block-wide scan of the lengths inside
-// every CTA (or, for batches of more than 2048 units, from a one-CTA prologue).
+// the N = 8 dimension, so each K/V byte is read once for the whole group. At a
+// split's end the CTA merges its warps' states in shared memory (warp order)
+// into one partial record per split. A second, small kernel (one CTA per unit
+// and query head, launched to overlap the first one's end) merges every unit's
+// records in split order into the output: records are indexed by split, so the
+// result does not depend on which CTA ran which split, and no merge waits on a
+// streaming CTA. The unit order and split offsets come from scans of the
+// lengths inside every CTA (batches of up to kMaxScanUnits units), or from a
+// one-CTA prologue for larger batches.
 // After a device error the workspace must be zero-filled again before reuse.
 #include <cuda_bf16.h>
 
@@ -33,17 +42,52 @@ constexpr int kConsumerWarps = 4;
 constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
 constexpr int kDecCtasPerSm = 2;
-constexpr int kSlotHeads = 8;  // partial records are padded to 8 heads
-constexpr int kMaxScanUnits = 2048;  // units whose offsets a CTA scans itself
-constexpr int kMinTokensPerCta = 512;  // small calls use fewer CTAs (the rest exit at once)
+constexpr int kMaxScanUnits = 512;     // units whose plan a CTA computes itself
+constexpr int kUnitBits = 9;           // scan tables pack (len << kUnitBits) | unit
+#ifndef CSMKV_DEC_ITEMS
+#define CSMKV_DEC_ITEMS 8
+#endif
+#ifndef CSMKV_DEC_MAX_SPLITS
+#define CSMKV_DEC_MAX_SPLITS 64
+#endif
+constexpr int kItemsPerCta = CSMKV_DEC_ITEMS;           // splits per equal share of the GPU
+constexpr int kMinSplit = 256;                          // tokens (4 tiles: per-split costs stay small)
+constexpr int kMaxSplitsPerUnit = CSMKV_DEC_MAX_SPLITS;  // bounds the records one unit's merge reads
+constexpr uint32_t kFirst = 1u, kLast = 2u;
+constexpr int kSlotHeads = 8;          // query heads of a group the MMA covers (N = 8)
+#ifndef CSMKV_DEC_CLAIM_EARLY
+#define CSMKV_DEC_CLAIM_EARLY 0
+#endif
 
-// Tokens per CTA for `total` tokens on a grid of n CTAs: an equal share, but at
-// least kMinTokensPerCta, so a small call does not spread a few tiles over
-// hundreds of CTAs and then merge hundreds of partial records.
-__host__ __device__ __forceinline__ int tokens_per_cta(int total, int n) {
-    const int share = (total + n - 1) / n;
-    return share > kMinTokensPerCta ? share : kMinTokensPerCta;
+// Base split length for `total` tokens on n CTAs: about kItemsPerCta splits per
+// CTA, a multiple of the tile, at least kMinSplit. Since S >= total / (n *
+// kItemsPerCta), a call has at most n * kItemsPerCta + units splits.
+__host__ __device__ __forceinline__ int split_base(long long total, int n) {
+    const long long per = (long long)n * kItemsPerCta;
+    long long s = (total + per - 1) / per;
+    s = (s + kTile - 1) / kTile * kTile;
+    return (int)(s > kMinSplit ? s : kMinSplit);
 }
+// Split length of a unit of `len` rows (of `total` over n CTAs): the base S, or
+// longer for a long unit, so that it has at most kMaxSplitsPerUnit splits -- or,
+// if it alone is a large part of the call, about one split per CTA of its share.
+// (The share is taken in fp32: the same operations give the same result in
+// every CTA and in the prologue.)
+__device__ __forceinline__ int unit_split(int len, int S, int total, int n) {
+    int cap = total > 0 ? (int)((float)n * ((float)len / (float)total)) : 0;
+    if (cap < kMaxSplitsPerUnit) cap = kMaxSplitsPerUnit;
+    unsigned su = ((unsigned)len + (unsigned)cap - 1u) / (unsigned)cap;
+    su = (su + kTile - 1u) / kTile * kTile;
+    return (int)su > S ? (int)su : S;
+}
+__device__ __forceinline__ int unit_nsplit(int len, int su) { return (len + su - 1) / su; }
+// Ticket order: units whose splits were lengthened first (long units: the
+// longest splits and merges), then units with many splits, then the rest.
+__device__ __forceinline__ int unit_class(int n, int su, int S) {
+    return su > S ? 0 : (n >= 16 ? 1 : (n >= 4 ? 2 : 3));
+}
+
+__host__ __device__ __forceinline__ int dec_max_splits(int nCTA, int BH) { return nCTA * kItemsPerCta + BH; }
 
 struct DecParams {
     const void* q;
@@ -58,13 +102,15 @@ struct DecParams {
     int32_t* len_rw;      // the same array as len
     void* out;
     WsHeader* hdr;
-    int32_t* prefix;      // [BH + 1] token offset of every unit
-    int32_t* cta_unit;    // [nCTA] first unit of every CTA's range (BH = none)
-    float* pm;            // [slots][8] running max (base-2 domain)
-    float* pl;            // [slots][8] running sum
-    float* pacc;          // [slots][8][D] unnormalised output
-    int32_t* counter;     // [BH] parts of a unit finished in this call; the last one resets it
-    int32_t BH, Hkv, Hq, G, cap, D, nCTA;
+    int32_t* g_first;     // [BH] first split of every unit (written by the plan)
+    int32_t* g_n;         // [BH] splits of every unit
+    int32_t* g_sp;        // prologue path: [BH + 1] first split of every unit
+    int32_t* g_len;       // prologue path: [BH] rows attended per unit
+    int32_t* g_unit;      // prologue path: [max splits] unit of every split
+    float* pm;            // [splits][G] running max (base-2 domain)
+    float* pl;            // [splits][G] running sum
+    float* pacc;          // [splits][G][D] unnormalised output
+    int32_t BH, Hkv, Hq, G, cap, D, nCTA, max_splits;
     float scale_log2;     // scale * log2(e)
     float scale;          // natural-log scale (fp32 path)
 };
@@ -84,62 +130,81 @@ __device__ __forceinline__ int eff_len(const DecParams& p, int u, bool record) {
     return v;
 }
 
+// Exclusive scan of 8 counters per thread over the block (threads in index
+// order); tot gets the block totals. scratch: one row of 8 per warp.
+__device__ __forceinline__ void block_scan8(int (&v)[8], int (&tot)[8], int (*scratch)[8]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        incl[i] = v[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl[i], o);
+            if (lane >= o) incl[i] += x;
+        }
+        if (lane == 31) scratch[warp][i] = incl[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int base = 0, t = 0;
+        for (int w = 0; w < nw; ++w) {
+            const int x = scratch[w][i];
+            if (w < warp) base += x;
+            t += x;
+        }
+        v[i] = base + incl[i] - v[i];
+        tot[i] = t;
+    }
+    __syncthreads();  // scratch may be reused
+}
+
 // ----------------------------------------------------------------------------
-// Prologue (one CTA): prefix sums of the lengths, tokens per CTA, first unit of
-// every CTA's range.
+// Prologue (one CTA, batches of more than kMaxScanUnits units): rows per unit,
+// the base split length, every unit's first split and split count (units in
+// index order) and the unit of every split.
 __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p) {
     griddep_launch_dependents();  // the main kernel may set itself up meanwhile
-    __shared__ int wsum[32];
+    __shared__ int scratch[32][8];
     __shared__ int carry_s;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry_s = 0;
+    const int tid = threadIdx.x;
+    long long total = 0;
+    for (int base = 0; base < p.BH; base += 1024) {
+        const int u = base + tid;
+        int v[8] = {u < p.BH ? eff_len(p, u, true) : 0, 0, 0, 0, 0, 0, 0, 0}, t[8];
+        if (u < p.BH) p.g_len[u] = v[0];
+        block_scan8(v, t, scratch);
+        total += t[0];
+    }
+    const int S = split_base(total, p.nCTA);
+    if (tid == 0) {
+        carry_s = 0;
+        p.hdr->dec_total = (int32_t)total;
+    }
+    const int total32 = (int)total;
     __syncthreads();
     for (int base = 0; base < p.BH; base += 1024) {
         const int u = base + tid;
-        const int v = u < p.BH ? eff_len(p, u, true) : 0;
-        int incl = v;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
-        }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int w = wsum[lane];
-            for (int o = 1; o < 32; o <<= 1) {
-                const int x = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += x;
-            }
-            wsum[lane] = w;  // inclusive over warps
+        const int len = u < p.BH ? p.g_len[u] : 0;
+        const int n = len > 0 ? unit_nsplit(len, unit_split(len, S, total32, p.nCTA)) : 0;
+        int v[8] = {n, 0, 0, 0, 0, 0, 0, 0}, t[8];
+        block_scan8(v, t, scratch);
+        const int first = carry_s + v[0];
+        if (u < p.BH) {
+            p.g_sp[u] = first;
+            p.g_first[u] = first;
+            p.g_n[u] = n;
+            for (int k = 0; k < n; ++k) p.g_unit[first + k] = u;
         }
         __syncthreads();
-        const int carry = carry_s;
-        const int excl = carry + incl - v + (warp ? wsum[warp - 1] : 0);
-        if (u < p.BH) p.prefix[u] = excl;
-        __syncthreads();
-        if (tid == 1023) carry_s = excl + v;
+        if (tid == 0) carry_s += t[0];
         __syncthreads();
     }
-    const int total = carry_s;
-    if (tid == 0) p.prefix[p.BH] = total;
-    const int W = tokens_per_cta(total, p.nCTA);
     if (tid == 0) {
-        p.hdr->total_tokens = total;
-        p.hdr->tokens_per_cta = W;
-    }
-    __syncthreads();
-    for (int c = tid; c < p.nCTA; c += 1024) {
-        const long long start = (long long)c * W;
-        int lo = 0, hi = p.BH;  // first unit with prefix[u+1] > start
-        if (start >= total) {
-            lo = p.BH;
-        } else {
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (p.prefix[mid + 1] > start) hi = mid; else lo = mid + 1;
-            }
-        }
-        p.cta_unit[c] = lo;
+        p.g_sp[p.BH] = carry_s;
+        p.hdr->dec_nsplits = carry_s;
+        p.hdr->dec_split = S;
     }
 }
 
@@ -150,26 +215,13 @@ struct DecGeom {
     static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kBoxes * kBoxBytes;
-    static constexpr int kNOff = 2 * kBoxes * kBoxBytes;
-    static constexpr int kNBytes = (kTile + 4) * 4;            // 68 degrees (row rounded down to 4)
-    static constexpr int kStageBytes = kNOff + 1024;           // keeps stages 1024-aligned
-    static constexpr uint32_t kTxBytes = 2 * kBoxes * kBoxBytes + kNBytes;
-};
-
-// Walks a CTA's token range as (unit, first token, token count) segments.
-struct RangeWalker {
-    const int32_t* prefix;
-    int BH, u, tok, end;
-    __device__ bool next(int& unit, int& t0, int& n) {
-        while (u < BH && prefix[u + 1] <= tok) ++u;
-        if (tok >= end || u >= BH) return false;
-        const int seg_end = min(end, prefix[u + 1]);
-        unit = u;
-        t0 = tok - prefix[u];
-        n = seg_end - tok;
-        tok = seg_end;
-        return true;
-    }
+    static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K and V boxes; 1024-aligned
+    static constexpr int kNBytes = (kTile / 4 + 1) * 16;       // 68 degrees (row rounded down to 4)
+    static constexpr int kNStride = 384;                       // degree tiles after the ring
+    static constexpr uint32_t kTxBytes = kStageBytes + kNBytes;
+    static constexpr int kQBytes = kSlotHeads * D * 2;          // the group's query rows (first tile of a split)
+    static constexpr int kQOff = kStages * kStageBytes + kStages * kNStride;
+    static constexpr int kSmallOff = kQOff + kStages * kQBytes;
 };
 
 // Shared scratch for merging partial softmax states: per-warp head maxima and
@@ -183,134 +235,192 @@ struct CombineScratch {
     float acc[kSlotHeads][kRedStride];
 };
 
+// What a stage holds: which split, which unit, where in the unit.
+struct StageMeta {
+    int32_t t;      // split (ticket); < 0: no more work
+    int32_t unit;
+    int32_t k;      // split index within the unit
+    int32_t n;      // splits of the unit
+    int32_t tok;    // first token of the tile within the unit
+    int32_t nv;     // valid tokens in the tile
+    uint32_t flags; // kFirst / kLast tile of the split
+    int32_t pad;
+};
+
 // Scratch of the main kernel after the stage ring.
 struct DecSmall {
     CombineScratch cs;
+    StageMeta meta[kStages];
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    int scan[kDecThreads / 32][8];
     int abort_flag;
-    int last;      // this CTA is the last contributor of the unit being closed
-    int bump;      // fused append: this CTA finished last and bumps the lengths
-    int u0;        // first unit of the CTA's range
+    int nsplits;
+    int S;
     int total;
-    int warp_tot[kDecThreads / 32];
 };
 
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
-    return old;
-}
+// One split, resolved from its ticket.
+struct Split {
+    int t, u, k, n, len, su;
+};
 
 __device__ __forceinline__ void consumer_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Merges the partials of `unit` -- one record per contributing CTA c0..c1, a
-// contiguous run -- into the output; run by the 4 consumer warps of the last
-// contributing CTA, so it sits on the kernel's tail: records are spread over
-// all 128 threads with several loads in flight per thread, and the cross-warp
-// sums go through shared memory in warp order (deterministic).
+// Barrier over the consumer warps that also ORs a predicate: every consumer
+// thread gets the same answer, so all of them take the same branch after it.
+__device__ __forceinline__ bool consumer_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, 1, %2, q;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Ticket -> split. SCAN: the CTA's own tables (positions in ticket order: sp =
+// first split, ulen = len << kUnitBits | unit); otherwise the prologue's
+// global tables (units in index order, g_unit maps a split to its unit).
+template <bool SCAN>
+__device__ __forceinline__ Split resolve_split(const DecParams& p, int t, int nsplits, int S, int total,
+                                               const int* sp, const uint32_t* ulen) {
+    Split r;
+    r.t = -1;
+    if (t < 0 || t >= nsplits) return r;
+    int first, last1;
+    if constexpr (SCAN) {
+        int lo = 0, hi = p.BH;  // last position with sp[pos] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (sp[mid] <= t) lo = mid; else hi = mid;
+        }
+        const uint32_t x = ulen[lo];
+        r.u = (int)(x & ((1u << kUnitBits) - 1u));
+        r.len = (int)(x >> kUnitBits);
+        first = sp[lo];
+        last1 = sp[lo + 1];
+    } else {
+        r.u = __ldcg(p.g_unit + t);
+        r.len = __ldcg(p.g_len + r.u);
+        first = __ldcg(p.g_sp + r.u);
+        last1 = __ldcg(p.g_sp + r.u + 1);
+    }
+    r.t = t;
+    r.k = t - first;
+    r.n = last1 - first;
+    r.su = unit_split(r.len, S, total, p.nCTA);
+    return r;
+}
+
+// Merges the split records of every unit into the output, one CTA per (unit,
+// query head of the group). Each thread owns 4 output columns and every RL-th
+// record of the unit; it loads up to kCombBatch of its records at once (all
+// loads in flight before any arithmetic: the records sit in L2, possibly on the
+// other die, so a dependent chain would pay the full latency per record), folds
+// them in split order with a running maximum, and the RL partial states are
+// merged in a fixed order (deterministic). Empty units get a zero output. After
+// its merge, the CTA for (0, 0) resets the split ticket for the next call and,
+// with a fused append, moves every length past its new token: the main kernel,
+// which read the lengths, has completed when griddepcontrol.wait returns.
+constexpr int kCombThreads = 256;
+constexpr int kCombBatch = 8;
 template <int D>
-__device__ void combine_unit(const DecParams& p, int unit, int c0, int c1, int warp, int lane, CombineScratch& cs) {
-    constexpr int PER = D / 32;  // dims per lane
-    const int tid = warp * 32 + lane;
-    const int G = p.G;
-    const int nrec = c1 - c0 + 1;
-    const size_t rec0 = (size_t)c0 + unit;
-
-    // pass 1: per-head maximum over the records
-    float mx[kSlotHeads];
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecParams p) {
+    constexpr int C4 = D / 4;              // float4 columns of one head
+    constexpr int RL = kCombThreads / C4;  // record lanes: 8 (D = 128) or 16 (D = 64)
+    __shared__ float sm_m[RL], sm_l[RL];
+    __shared__ float4 sm_acc[RL][C4];
+    griddep_launch_dependents();  // the next kernel may set itself up meanwhile
+    griddep_wait();
+    const int u = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+    const int first = p.g_first[u], n = p.g_n[u];
+    const int b = u / p.Hkv, kv = u - b * p.Hkv;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D;
+    if (n <= 0) {
+        for (int i = tid; i < D / 8; i += kCombThreads) reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        const int c = tid % C4, rl = tid / C4;
+        float m = -INFINITY, l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r0 = rl; r0 < n; r0 += RL * kCombBatch) {
+            float pmv[kCombBatch], plv[kCombBatch];
+            float4 v[kCombBatch];
 #pragma unroll
-    for (int g = 0; g < kSlotHeads; ++g) mx[g] = -INFINITY;
-    for (int r = tid; r < nrec; r += kConsumerWarps * 32) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.pm + (rec0 + r) * kSlotHeads));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(p.pm + (rec0 + r) * kSlotHeads + 4));
-        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int g = 0; g < kSlotHeads; ++g)
-            if (g < G) mx[g] = fmaxf(mx[g], v[g]);
-    }
-#pragma unroll
-    for (int g = 0; g < kSlotHeads; ++g) {
-#pragma unroll
-        for (int o = 16; o; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < kSlotHeads; ++g) cs.m[warp][g] = mx[g];
-    }
-    consumer_barrier();
-    float M[kSlotHeads];
-#pragma unroll
-    for (int g = 0; g < kSlotHeads; ++g) M[g] = fmaxf(fmaxf(cs.m[0][g], cs.m[1][g]), fmaxf(cs.m[2][g], cs.m[3][g]));
-
-    // pass 2: warp w folds records w, w+4, ...; lane covers PER dims of every head
-    float acc[kSlotHeads][PER], L[kSlotHeads];
-#pragma unroll
-    for (int g = 0; g < kSlotHeads; ++g) {
-        L[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) acc[g][i] = 0.f;
-    }
-#pragma unroll 4
-    for (int r = warp; r < nrec; r += kConsumerWarps) {
-        const size_t rec = rec0 + r;
-        const float4 ma = __ldcg(reinterpret_cast<const float4*>(p.pm + rec * kSlotHeads));
-        const float4 mb = __ldcg(reinterpret_cast<const float4*>(p.pm + rec * kSlotHeads + 4));
-        const float4 la = __ldcg(reinterpret_cast<const float4*>(p.pl + rec * kSlotHeads));
-        const float4 lb = __ldcg(reinterpret_cast<const float4*>(p.pl + rec * kSlotHeads + 4));
-        const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-#pragma unroll
-        for (int g = 0; g < kSlotHeads; ++g) {
-            if (g < G) {
-                // a CTA that saw no token of a head left m = -inf, l = 0, acc = 0
-                const float f = mv[g] == -INFINITY ? 0.f : exp2f(mv[g] - M[g]);
-                L[g] = fmaf(f, lv[g], L[g]);
-                const float* a = p.pacc + (rec * kSlotHeads + g) * D + lane * PER;
-                if constexpr (PER == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(a));
-                    acc[g][0] = fmaf(f, v.x, acc[g][0]);
-                    acc[g][1] = fmaf(f, v.y, acc[g][1]);
-                    acc[g][2] = fmaf(f, v.z, acc[g][2]);
-                    acc[g][3] = fmaf(f, v.w, acc[g][3]);
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2*>(a));
-                    acc[g][0] = fmaf(f, v.x, acc[g][0]);
-                    acc[g][1] = fmaf(f, v.y, acc[g][1]);
+            for (int j = 0; j < kCombBatch; ++j) {
+                const int r = r0 + j * RL;
+                pmv[j] = -INFINITY;
+                plv[j] = 0.f;
+                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < n) {
+                    const size_t rec = (size_t)(first + r) * p.G + g;
+                    pmv[j] = __ldcg(p.pm + rec);
+                    plv[j] = __ldcg(p.pl + rec);
+                    v[j] = __ldcg(reinterpret_cast<const float4*>(p.pacc + rec * D) + c);
                 }
             }
-        }
-    }
-
-    // cross-warp sums in warp order
-    for (int w = 0; w < kConsumerWarps; ++w) {
-        if (warp == w) {
 #pragma unroll
-            for (int g = 0; g < kSlotHeads; ++g) {
-                if (g < G) {
-                    float* row = &cs.acc[g][lane * PER];
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) row[i] = (w == 0) ? acc[g][i] : row[i] + acc[g][i];
-                    if (lane == 0) cs.l[w][g] = L[g];
-                }
+            for (int j = 0; j < kCombBatch; ++j) {
+                // a record of a head that saw no token holds m = -inf, l = 0, acc = 0
+                if (pmv[j] == -INFINITY) continue;
+                const float mn = fmaxf(m, pmv[j]);
+                const float a = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+                const float f = exp2f(pmv[j] - mn);
+                l = fmaf(f, plv[j], l * a);
+                acc.x = fmaf(f, v[j].x, acc.x * a);
+                acc.y = fmaf(f, v[j].y, acc.y * a);
+                acc.z = fmaf(f, v[j].z, acc.z * a);
+                acc.w = fmaf(f, v[j].w, acc.w * a);
+                m = mn;
             }
         }
-        consumer_barrier();
+        if (c == 0) {
+            sm_m[rl] = m;
+            sm_l[rl] = l;
+        }
+        sm_acc[rl][c] = acc;
+        __syncthreads();
+        if (rl == 0) {
+            float M = sm_m[0];
+#pragma unroll
+            for (int k = 1; k < RL; ++k) M = fmaxf(M, sm_m[k]);
+            float L = 0.f;
+            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < RL; ++k) {
+                if (sm_m[k] == -INFINITY) continue;
+                const float f = exp2f(sm_m[k] - M);
+                const float4 x = sm_acc[k][c];
+                L = fmaf(f, sm_l[k], L);
+                A.x = fmaf(f, x.x, A.x);
+                A.y = fmaf(f, x.y, A.y);
+                A.z = fmaf(f, x.z, A.z);
+                A.w = fmaf(f, x.w, A.w);
+            }
+            const float inv = 1.0f / L;
+            *reinterpret_cast<uint2*>(o + 4 * c) =
+                make_uint2(pack_bf16x2(A.x * inv, A.y * inv), pack_bf16x2(A.z * inv, A.w * inv));
+        }
     }
-    const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
-    for (int i = tid; i < G * (D / 4); i += kConsumerWarps * 32) {
-        const int g = i / (D / 4), d = (i - g * (D / 4)) * 4;
-        const float inv = 1.0f / ((cs.l[0][g] + cs.l[1][g]) + (cs.l[2][g] + cs.l[3][g]));
-        const float4 v = *reinterpret_cast<const float4*>(&cs.acc[g][d]);
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * G + g) * D + d;
-        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(v.x * inv, v.y * inv), pack_bf16x2(v.z * inv, v.w * inv));
+    if (u == 0 && g == 0) {
+        if (tid == 0) p.hdr->ticket = 0;
+        if (p.k_new) {
+            for (int x = tid; x < p.BH; x += kCombThreads) {
+                const int v = p.len[x];
+                if (v >= 0 && v < p.cap) p.len_rw[x] = v + 1;
+            }
+        }
     }
 }
 
-// SCAN: the CTA computes the unit offsets itself (units <= kMaxScanUnits, kept in
-// shared memory); otherwise decode_prologue_kernel has written them to the workspace.
+// SCAN: the CTA computes the unit order and split offsets itself (units <=
+// kMaxScanUnits, kept in shared memory); otherwise decode_prologue_kernel has
+// written them to the workspace.
 template <int D, bool SCAN>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     decode_main_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tmK,
@@ -319,13 +429,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* const sbase =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    DecSmall& sm = *reinterpret_cast<DecSmall*>(sbase + kStages * Geo::kStageBytes);
-    int* const sPrefix = reinterpret_cast<int*>(&sm + 1);
+    uint8_t* const nbase = sbase + kStages * Geo::kStageBytes;
+    DecSmall& sm = *reinterpret_cast<DecSmall*>(sbase + Geo::kSmallOff);
+    int* const sp = reinterpret_cast<int*>(&sm + 1);                      // [kMaxScanUnits + 1]
+    uint32_t* const ulen = reinterpret_cast<uint32_t*>(sp + kMaxScanUnits + 1);  // [kMaxScanUnits]
     uint64_t* const full = sm.full;
     uint64_t* const empty = sm.empty;
     volatile int* const abort_flag = &sm.abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint64_t budget_ns = 2000000000ull;
 
     // Private setup first; then wait for the previous kernel in the stream (its
     // lengths, cache rows and workspace state) before reading anything.
@@ -333,212 +446,258 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmN);
-    }
-    griddep_launch_dependents();
-    griddep_wait();
-
-    // ---------------------------------------------------------------- unit offsets
-    const int* pre;
-    int total, W;
-    if constexpr (SCAN) {
-        const int per = (p.BH + kDecThreads - 1) / kDecThreads;
-        const int ub = tid * per;
-        int local = 0;
-        for (int i = 0; i < per; ++i) {
-            const int u = ub + i;
-            if (u < p.BH) local += eff_len(p, u, true);
-        }
-        int incl = local;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
-        }
-        if (lane == 31) sm.warp_tot[warp] = incl;
-        __syncthreads();
-        if (tid == 0) {
-            int run = 0;
-            for (int w = 0; w < kDecThreads / 32; ++w) {
-                const int t = sm.warp_tot[w];
-                sm.warp_tot[w] = run;
-                run += t;
-            }
-            sm.total = run;
-            sPrefix[p.BH] = run;
-        }
-        __syncthreads();
-        int run = sm.warp_tot[warp] + incl - local;
-        for (int i = 0; i < per; ++i) {
-            const int u = ub + i;
-            if (u < p.BH) {
-                sPrefix[u] = run;
-                run += eff_len(p, u, false);
-            }
-        }
-        __syncthreads();
-        pre = sPrefix;
-        total = sm.total;
-        W = tokens_per_cta(total, (int)gridDim.x);
-    } else {
-        pre = p.prefix;
-        total = p.hdr->total_tokens;
-        W = p.hdr->tokens_per_cta;
-    }
-
-    // Empty units get a zero output from the CTA whose range starts at their offset.
-    for (int u = tid; u < p.BH; u += kDecThreads) {
-        if (pre[u + 1] != pre[u]) continue;
-        if (min(pre[u] / W, (int)gridDim.x - 1) != (int)blockIdx.x) continue;
-        const int b = u / p.Hkv, kv = u - b * p.Hkv;
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((size_t)b * p.Hq + (size_t)kv * p.G) * D;
-        for (int i = 0; i < p.G * D / 8; ++i) reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-
-    const int r0 = blockIdx.x * W;
-    const int r1 = min(total, r0 + W);
-    // Fused append: once every CTA is done (and so done reading len), the last one
-    // moves every unit's length past its new token.
-    auto finish_append = [&](int nthr, bool block_sync) {
-        if (!p.k_new) return;
-        if (tid == 0) sm.bump = atomicAdd(&p.hdr->ctas_done, 1) == (int)gridDim.x - 1;
-        if (block_sync) __syncthreads(); else consumer_barrier();
-        if (!sm.bump) return;
-        for (int u = tid; u < p.BH; u += nthr) {
-            const int v = p.len[u];
-            if (v >= 0 && v < p.cap) p.len_rw[u] = v + 1;
-        }
-        if (tid == 0) p.hdr->ctas_done = 0;
-    };
-    if (r0 >= r1) {
-        finish_append(kDecThreads, true);
-        return;
-    }
-    int u0;
-    if constexpr (SCAN) {
-        if (tid == 0) sm.u0 = p.BH;
-        __syncthreads();
-        for (int u = tid; u < p.BH; u += kDecThreads)
-            if (pre[u] <= r0 && r0 < pre[u + 1]) sm.u0 = u;
-        __syncthreads();
-        u0 = sm.u0;
-    } else {
-        u0 = p.cta_unit[blockIdx.x];
-    }
-    int u0_last = u0;  // unit holding the range's last token
-    if (p.k_new)
-        while (u0_last + 1 < p.BH && pre[u0_last + 1] < r1) ++u0_last;
-
-    // Fused append: the CTA whose range holds a unit's last row (the new token)
-    // writes that row before any of its loads, 2 * D / 8 sixteen-byte pieces per
-    // unit spread over the block; the fence orders the writes before the TMA reads.
-    if (p.k_new) {
-        constexpr int PPR = D / 8;  // 16-byte pieces per row
-        for (int i = tid; i < (u0_last - u0 + 1) * 2 * PPR; i += kDecThreads) {
-            const int u = u0 + i / (2 * PPR), k = i % (2 * PPR);
-            const int old = p.len[u];
-            if (old < 0 || old >= p.cap || pre[u + 1] - 1 < r0 || pre[u + 1] - 1 >= r1) continue;
-            const size_t r = (size_t)u * p.cap + old;
-            const bool isv = k >= PPR;
-            const uint4* src = static_cast<const uint4*>(isv ? p.v_new : p.k_new) + (size_t)u * PPR + (k % PPR);
-            uint4* dst = static_cast<uint4*>(isv ? p.V : p.K) + r * PPR + (k % PPR);
-            *dst = *src;
-            if (k == 0) p.N[r] = 1;
-            fence_proxy_async_global();
-        }
-    }
-    if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
-        prefetch_tmap(&tmN);
+    }
+    griddep_launch_dependents();
+    griddep_wait();
+
+    // ---------------------------------------------------------------- split plan
+    if constexpr (SCAN) {
+        // One warp plans the call with shuffles only: every lane holds the rows of
+        // up to kPer consecutive units (all loads in flight at once).
+        if (warp == 0) {
+            constexpr int kPer = kMaxScanUnits / 32;
+            const int per = (p.BH + 31) / 32;
+            const int ub = lane * per;
+            int lr[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) lr[i] = (i < per && ub + i < p.BH) ? eff_len(p, ub + i, true) : 0;
+            int total = 0;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) total += lr[i];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+            const int S = split_base(total, (int)gridDim.x);
+            // units and splits per class, then positions: classes in order, units in
+            // index order inside a class
+            int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                if (i < per && ub + i < p.BH) {
+                    const int len = lr[i];
+                    const int su = len > 0 ? unit_split(len, S, total, p.nCTA) : S;
+                    const int n = len > 0 ? unit_nsplit(len, su) : 0;
+                    const int cls = n > 0 ? unit_class(n, su, S) : 3;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (k == cls) {
+                            c[k] += 1;
+                            c[4 + k] += n;
+                        }
+                    }
+                }
+            }
+            int upos[4], spos[4], ru = 0, rs = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                int incl = c[k];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                if (k < 4) {
+                    upos[k] = ru + incl - c[k];
+                    ru += tot;
+                } else {
+                    spos[k - 4] = rs + incl - c[k];
+                    rs += tot;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int u = ub + i;
+                if (i < per && u < p.BH) {
+                    const int len = lr[i];
+                    const int su = len > 0 ? unit_split(len, S, total, p.nCTA) : S;
+                    const int n = len > 0 ? unit_nsplit(len, su) : 0;
+                    const int cls = n > 0 ? unit_class(n, su, S) : 3;
+                    int pos = 0, first = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (k == cls) {
+                            pos = upos[k]++;
+                            first = spos[k];
+                            spos[k] += n;
+                        }
+                    }
+                    sp[pos] = first;
+                    ulen[pos] = ((uint32_t)len << kUnitBits) | (uint32_t)u;
+                    if (blockIdx.x == 0) {  // for the merge kernel
+                        p.g_first[u] = first;
+                        p.g_n[u] = n;
+                    }
+                }
+            }
+            if (lane == 0) {
+                sp[p.BH] = rs;
+                sm.nsplits = rs;
+                sm.S = S;
+                sm.total = total;
+            }
+        }
+    } else {
+        if (tid == 0) {
+            sm.nsplits = p.hdr->dec_nsplits;
+            sm.S = p.hdr->dec_split;
+            sm.total = p.hdr->dec_total;
+        }
     }
     __syncthreads();
-    const uint64_t budget_ns = 2000000000ull;
+    const int nsplits = sm.nsplits, S = sm.S, total = sm.total;
 
     if (warp == kConsumerWarps) {
         // ============================================================ producer
-        if (lane == 0) {
-            int issued = 0;
-            RangeWalker rw{pre, p.BH, u0, r0, r1};
-            int unit, t0, n;
-            bool ok = true;
-            while (ok && rw.next(unit, t0, n)) {
-                const long long row_base = (long long)unit * p.cap;
-                for (int t = 0; t < n; t += kTile) {
-                    const int s = issued % kStages;
-                    if (issued >= kStages) {
-                        ok = mbar_wait(&empty[s], ((issued / kStages) - 1) & 1, globaltimer() + budget_ns);
-                        if (!ok || *abort_flag) { ok = false; break; }
+        int issued = 0;
+        bool ok = true;
+        // split blockIdx.x first; later splits come from the ticket, from gridDim.x on
+        Split cur = resolve_split<SCAN>(p, (int)blockIdx.x, nsplits, S, total, sp, ulen);
+        while (cur.t >= 0) {
+            int tn = 0;
+            const int tok0 = cur.k * cur.su;
+            const int ntok = min(cur.su, cur.len - tok0);
+            const int ntiles = (ntok + kTile - 1) / kTile;
+            const long long row_base = (long long)cur.u * p.cap;
+            int arow = -1;  // fused append: the unit's new row, held by its last split
+            if (p.k_new && cur.k == cur.n - 1) {
+                const int old = p.len[cur.u];
+                if (old >= 0 && old < p.cap) arow = old;
+            }
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = issued % kStages;
+                // the next split is claimed with the last tile of this one: the ring
+                // still holds up to kStages tiles of work while the ticket and its
+                // plan resolve, and no split is held longer than that before it starts
+#if CSMKV_DEC_CLAIM_EARLY
+                if (i == 0 && lane == 0) tn = (int)gridDim.x + atomicAdd(&p.hdr->ticket, 1);
+#else
+                if (i == ntiles - 1 && lane == 0) tn = (int)gridDim.x + atomicAdd(&p.hdr->ticket, 1);
+#endif
+                if (issued >= kStages) {
+                    int w = 1;
+                    if (lane == 0)
+                        w = mbar_wait(&empty[s], ((issued / kStages) - 1) & 1, globaltimer() + budget_ns) && !*abort_flag;
+                    if (!__shfl_sync(0xffffffffu, w, 0)) {
+                        ok = false;
+                        break;
                     }
-                    const int row = (int)(row_base + t0 + t);
+                }
+                const int tok = tok0 + i * kTile;
+                const int nv = min(kTile, ntok - i * kTile);
+                if (arow >= tok && arow < tok + nv) {
+                    // the new token's K, V row and degree, written before the TMA reads the
+                    // tile (one 16-byte piece per lane; the fence orders each lane's writes
+                    // before the async-proxy reads that follow the warp sync)
+                    constexpr int PPR = D / 8;
+                    if (lane < 2 * PPR) {
+                        const bool isv = lane >= PPR;
+                        const int kk = isv ? lane - PPR : lane;
+                        const uint4* src = static_cast<const uint4*>(isv ? p.v_new : p.k_new) + (size_t)cur.u * PPR + kk;
+                        uint4* dst = static_cast<uint4*>(isv ? p.V : p.K) + (size_t)(row_base + arow) * PPR + kk;
+                        *dst = *src;
+                        if (lane == 0) p.N[row_base + arow] = 1;
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    StageMeta& mt = sm.meta[s];
+                    mt.t = cur.t;
+                    mt.unit = cur.u;
+                    mt.k = cur.k;
+                    mt.n = cur.n;
+                    mt.tok = tok;
+                    mt.nv = nv;
+                    mt.flags = (i == 0 ? kFirst : 0u) | (i == ntiles - 1 ? kLast : 0u);
+                    const int row = (int)(row_base + tok);
                     uint8_t* st = sbase + s * Geo::kStageBytes;
-                    mbar_expect_tx(&full[s], Geo::kTxBytes);
+                    // the first tile of a split also brings the group's query rows
+                    const uint32_t qbytes = i == 0 ? (uint32_t)(p.G * D * 2) : 0u;
+                    mbar_expect_tx(&full[s], Geo::kTxBytes + qbytes);
+                    if (i == 0) {
+                        const int b = cur.u / p.Hkv, kv = cur.u - b * p.Hkv;
+                        bulk_load(sbase + Geo::kQOff + s * Geo::kQBytes,
+                                  static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + (size_t)kv * p.G) * D,
+                                  qbytes, &full[s]);
+                    }
 #pragma unroll
                     for (int bx = 0; bx < Geo::kBoxes; ++bx) {
                         tma_load_2d(st + Geo::kKOff + bx * Geo::kBoxBytes, &tmK, &full[s], bx * 64, row);
                         tma_load_2d(st + Geo::kVOff + bx * Geo::kBoxBytes, &tmV, &full[s], bx * 64, row);
                     }
-                    tma_load_2d(st + Geo::kNOff, &tmN, &full[s], 0, row >> 2);
-                    ++issued;
+                    tma_load_2d(nbase + s * Geo::kNStride, &tmN, &full[s], 0, row >> 2);
                 }
+                ++issued;
             }
-            if (!ok) {
-                record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
-                *abort_flag = 1;
+            if (!ok) break;
+            tn = __shfl_sync(0xffffffffu, tn, 0);
+            cur = resolve_split<SCAN>(p, tn, nsplits, S, total, sp, ulen);
+        }
+        if (ok) {
+            // stop marker for the consumers, in the stage after the last one issued
+            if (lane == 0) {
+                const int s = issued % kStages;
+                if (issued >= kStages)
+                    ok = mbar_wait(&empty[s], ((issued / kStages) - 1) & 1, globaltimer() + budget_ns);
+                sm.meta[s].t = -1;
+                if (ok) mbar_arrive(&full[s]);
             }
-            // Drain: every issued stage must land before the CTA may exit.
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+        }
+        if (!ok && lane == 0) {
+            record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
+            *abort_flag = 1;
+            // the consumers may stop early: every issued stage must land before the CTA exits
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 (void)mbar_wait(&full[i % kStages], (i / kStages) & 1, globaltimer() + budget_ns);
         }
         __syncwarp();
-        return;
-    }
-
-    // ================================================================ consumers
-    const int g = lane >> 2, t4 = lane & 3;
-    const int tok_lo = warp * 16;
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
-    uint32_t qf[D / 16][2];
-    float oacc[D / 16][4];
-    float m0, m1, l0, l1;
-
-    RangeWalker rw{pre, p.BH, u0, r0, r1};
-    int unit, t0, n;
-    int consumed = 0;
-    bool ok = true;
-    while (rw.next(unit, t0, n)) {
-        const int b = unit / p.Hkv, kv = unit - b * p.Hkv;
-        const __nv_bfloat16* qrow = qg + ((size_t)b * p.Hq + (size_t)kv * p.G + g) * D;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            if (g < p.G) {
-                qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4);
-                qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * t4);
-            } else {
-                qf[ks][0] = 0u;
-                qf[ks][1] = 0u;
-            }
-        }
-#pragma unroll
-        for (int mb = 0; mb < D / 16; ++mb) oacc[mb][0] = oacc[mb][1] = oacc[mb][2] = oacc[mb][3] = 0.f;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-        const long long row_base = (long long)unit * p.cap;
-
-        for (int t = 0; t < n; t += kTile) {
+    } else {
+        // ============================================================ consumers
+        const int g = lane >> 2, t4 = lane & 3;
+        const int tok_lo = warp * 16;
+        uint32_t qf[D / 16][2];
+        float oacc[D / 16][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int consumed = 0;
+        bool ok = true;
+        for (;;) {
             const int s = consumed % kStages;
-            if (!mbar_wait(&full[s], (consumed / kStages) & 1, globaltimer() + budget_ns) || *abort_flag) {
+            const bool got = mbar_wait(&full[s], (consumed / kStages) & 1, globaltimer() + budget_ns);
+            if (consumer_any(!got || *abort_flag)) {
                 ok = false;
                 break;
             }
-            const int nv = min(kTile, n - t);  // valid tokens in this tile
+            const StageMeta mt = sm.meta[s];
+            if (mt.t < 0) break;
+            if (mt.flags & kFirst) {  // the split's query rows came with this tile
+                const __nv_bfloat16* qrow =
+                    reinterpret_cast<const __nv_bfloat16*>(sbase + Geo::kQOff + s * Geo::kQBytes) + g * D;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    if (g < p.G) {
+                        qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4);
+                        qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * t4);
+                    } else {
+                        qf[ks][0] = 0u;
+                        qf[ks][1] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) oacc[mb][0] = oacc[mb][1] = oacc[mb][2] = oacc[mb][3] = 0.f;
+                m0 = m1 = -INFINITY;
+                l0 = l1 = 0.f;
+            }
+            const int nv = mt.nv;
             uint8_t* st = sbase + s * Geo::kStageBytes;
-            const int noff = (int)((row_base + t0 + t) & 3);
-            const int* sN = reinterpret_cast<const int*>(st + Geo::kNOff) + noff;
+            const int noff = (int)(((long long)mt.unit * p.cap + mt.tok) & 3);
+            const int* sN = reinterpret_cast<const int*>(nbase + s * Geo::kNStride) + noff;
             if (tok_lo < nv) {
                 // ---- S^T = K q^T (16 tokens x 8 heads)
                 float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -613,89 +772,73 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++consumed;
-        }
-        // ---- every consumer warp reaches the barriers below, aborted or not
-        if (!ok) *abort_flag = 1;
-        consumer_barrier();
-        if (*abort_flag) {
-            ok = false;
-            break;
-        }
-        // ---- one partial per (CTA, unit): the 4 warps' states merged in shared memory,
-        //      in warp order (deterministic), then written as one record
-        float lt0 = l0, lt1 = l1;
+            if (!(mt.flags & kLast)) continue;
+
+            // ---- end of a split: the 4 warps' states merged in shared memory, in warp
+            //      order (deterministic), then written as the split's record
+            float lt0 = l0, lt1 = l1;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
-            lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
-        }
-        CombineScratch& cs = sm.cs;
-        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-        if (g == 0) {
-            cs.m[warp][h0] = m0;
-            cs.m[warp][h1] = m1;
-            cs.l[warp][h0] = lt0;
-            cs.l[warp][h1] = lt1;
-        }
-        consumer_barrier();
-        {
-            const float M0 = fmaxf(fmaxf(cs.m[0][h0], cs.m[1][h0]), fmaxf(cs.m[2][h0], cs.m[3][h0]));
-            const float M1 = fmaxf(fmaxf(cs.m[0][h1], cs.m[1][h1]), fmaxf(cs.m[2][h1], cs.m[3][h1]));
-            const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-            const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                if (warp == w) {
+            for (int o = 4; o < 32; o <<= 1) {
+                lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+                lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+            }
+            CombineScratch& cs = sm.cs;
+            const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+            if (g == 0) {
+                cs.m[warp][h0] = m0;
+                cs.m[warp][h1] = m1;
+                cs.l[warp][h0] = lt0;
+                cs.l[warp][h1] = lt1;
+            }
+            consumer_barrier();
+            {
+                const float M0 = fmaxf(fmaxf(cs.m[0][h0], cs.m[1][h0]), fmaxf(cs.m[2][h0], cs.m[3][h0]));
+                const float M1 = fmaxf(fmaxf(cs.m[0][h1], cs.m[1][h1]), fmaxf(cs.m[2][h1], cs.m[3][h1]));
+                const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+                const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    if (warp == w) {
 #pragma unroll
-                    for (int mb = 0; mb < D / 16; ++mb) {
-                        float* r0 = &cs.acc[h0][16 * mb + g];
-                        float* r1 = &cs.acc[h1][16 * mb + g];
-                        if (w == 0) {
-                            r0[0] = f0 * oacc[mb][0];
-                            r1[0] = f1 * oacc[mb][1];
-                            r0[8] = f0 * oacc[mb][2];
-                            r1[8] = f1 * oacc[mb][3];
-                        } else {
-                            r0[0] = fmaf(f0, oacc[mb][0], r0[0]);
-                            r1[0] = fmaf(f1, oacc[mb][1], r1[0]);
-                            r0[8] = fmaf(f0, oacc[mb][2], r0[8]);
-                            r1[8] = fmaf(f1, oacc[mb][3], r1[8]);
+                        for (int mb = 0; mb < D / 16; ++mb) {
+                            float* r0 = &cs.acc[h0][16 * mb + g];
+                            float* r1 = &cs.acc[h1][16 * mb + g];
+                            if (w == 0) {
+                                r0[0] = f0 * oacc[mb][0];
+                                r1[0] = f1 * oacc[mb][1];
+                                r0[8] = f0 * oacc[mb][2];
+                                r1[8] = f1 * oacc[mb][3];
+                            } else {
+                                r0[0] = fmaf(f0, oacc[mb][0], r0[0]);
+                                r1[0] = fmaf(f1, oacc[mb][1], r1[0]);
+                                r0[8] = fmaf(f0, oacc[mb][2], r0[8]);
+                                r1[8] = fmaf(f1, oacc[mb][3], r1[8]);
+                            }
                         }
                     }
+                    consumer_barrier();
                 }
-                consumer_barrier();
             }
+            const size_t rec = (size_t)mt.t * p.G;
+            for (int i = tid; i < p.G * (D / 4); i += kConsumerWarps * 32) {
+                const int h = i / (D / 4), d = (i - h * (D / 4)) * 4;
+                __stcg(reinterpret_cast<float4*>(p.pacc + (rec + h) * D + d), *reinterpret_cast<const float4*>(&cs.acc[h][d]));
+            }
+            if (tid < p.G) {
+                const float M = fmaxf(fmaxf(cs.m[0][tid], cs.m[1][tid]), fmaxf(cs.m[2][tid], cs.m[3][tid]));
+                float L = 0.f;
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    if (cs.m[w][tid] != -INFINITY) L = fmaf(exp2f(cs.m[w][tid] - M), cs.l[w][tid], L);
+                p.pm[rec + tid] = M;
+                p.pl[rec + tid] = L;
+            }
+            // the merge scratch is next written at the end of a later split, after at
+            // least one more consumer barrier
         }
-        const size_t slot = (size_t)blockIdx.x + unit;
-        for (int i = tid; i < p.G * (D / 4); i += kConsumerWarps * 32) {
-            const int h = i / (D / 4), d = (i - h * (D / 4)) * 4;
-            __stcg(reinterpret_cast<float4*>(p.pacc + (slot * kSlotHeads + h) * D + d),
-                   *reinterpret_cast<const float4*>(&cs.acc[h][d]));
+        if (!ok && tid == 0) {
+            record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
+            *abort_flag = 1;
         }
-        if (tid < p.G) {
-            const float M = fmaxf(fmaxf(cs.m[0][tid], cs.m[1][tid]), fmaxf(cs.m[2][tid], cs.m[3][tid]));
-            float L = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w)
-                if (cs.m[w][tid] != -INFINITY) L = fmaf(exp2f(cs.m[w][tid] - M), cs.l[w][tid], L);
-            p.pm[slot * kSlotHeads + tid] = M;
-            p.pl[slot * kSlotHeads + tid] = L;
-        }
-        // ---- the last CTA to finish its part of the unit merges every part. One
-        //      acq_rel atomic both publishes this CTA's record (its stores are ordered
-        //      before it by the barrier) and, for the last CTA, acquires the others'.
-        consumer_barrier();
-        const int c0 = pre[unit] / W, c1 = (pre[unit + 1] - 1) / W;
-        if (tid == 0) {
-            const int prev = atom_add_acq_rel_gpu(p.counter + unit, 1);
-            const int last = prev == c1 - c0;
-            if (last) p.counter[unit] = 0;  // ready for the next call
-            sm.last = last;
-        }
-        consumer_barrier();
-        if (sm.last) combine_unit<D>(p, unit, c0, c1, warp, lane, sm.cs);
-        consumer_barrier();  // sm.last is rewritten for the next unit
     }
-    if (!ok && tid == 0) record_status(&p.hdr->status, CSMKV_ERR_TIMEOUT);
-    finish_append(kConsumerWarps * 32, false);
 }
 
 // ----------------------------------------------------------------------------
@@ -763,52 +906,46 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const DecParams p, cons
     }
 }
 
-static size_t dec_layout(const csmkv_cache* cache, int nCTA, size_t* o_prefix, size_t* o_cta, size_t* o_cnt,
-                         size_t* o_pm, size_t* o_pl, size_t* o_pacc) {
+static size_t dec_layout(const csmkv_cache* cache, int32_t h_q, int nCTA, size_t* o_first, size_t* o_n, size_t* o_sp,
+                         size_t* o_len, size_t* o_unit, size_t* o_pm, size_t* o_pl, size_t* o_pacc) {
     const size_t BH = (size_t)cache->batch * cache->h_kv;
-    const size_t slots = (size_t)nCTA + BH;  // one record per (CTA, unit it touches)
+    const size_t G = (size_t)h_q / cache->h_kv;
+    const size_t splits = (size_t)dec_max_splits(nCTA, (int)BH);  // one record per split
     size_t off = kHeaderBytes;
-    *o_prefix = off;
-    off = align_up(off + (BH + 1) * 4, 256);
-    *o_cta = off;
-    off = align_up(off + (size_t)nCTA * 4, 256);
-    *o_cnt = off;
+    *o_first = off;
     off = align_up(off + BH * 4, 256);
+    *o_n = off;
+    off = align_up(off + BH * 4, 256);
+    *o_sp = off;
+    off = align_up(off + (BH + 1) * 4, 256);
+    *o_len = off;
+    off = align_up(off + BH * 4, 256);
+    *o_unit = off;
+    off = align_up(off + splits * 4, 256);
     *o_pm = off;
-    off = align_up(off + slots * kSlotHeads * 4, 256);
+    off = align_up(off + splits * G * 4, 256);
     *o_pl = off;
-    off = align_up(off + slots * kSlotHeads * 4, 256);
+    off = align_up(off + splits * G * 4, 256);
     *o_pacc = off;
-    off = align_up(off + slots * kSlotHeads * (size_t)cache->head_dim * 4, 256);
+    off = align_up(off + splits * G * (size_t)cache->head_dim * 4, 256);
     return off;
 }
 
 template <int D, bool SCAN>
 static int launch_decode_bf16(const DecParams& P, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tn, cudaStream_t st) {
-    constexpr int smem = kStages * DecGeom<D>::kStageBytes + (int)sizeof(DecSmall) +
-                         (SCAN ? (kMaxScanUnits + 1) * 4 : 0) + 1024;
+    constexpr int smem = DecGeom<D>::kSmallOff + (int)sizeof(DecSmall) + (SCAN ? (2 * kMaxScanUnits + 1) * 4 : 0) +
+                         1024;
     static_assert(kDecCtasPerSm * (smem + 1024) <= 228 * 1024, "two CTAs per SM must fit in shared memory");
     auto kern = decode_main_kernel<D, SCAN>;
     if (set_kernel_smem((const void*)kern, smem) != CSMKV_OK) return CSMKV_ERR_CUDA;
     if (launch_overlapped(kern, dim3(P.nCTA), dim3(kDecThreads), (size_t)smem, st, P, tk, tv, tn) != cudaSuccess)
         return CSMKV_ERR_CUDA;
+    if (launch_overlapped(decode_combine_kernel<D>, dim3(P.BH, P.G), dim3(kCombThreads), 0, st, P) != cudaSuccess)
+        return CSMKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
 }
 
-}  // namespace csmkv
-
-using namespace csmkv;
-
-extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t h_q) {
-    if (check_cache(cache) != CSMKV_OK || h_q < 1) return 0;
-    const int nCTA = sm_count() * kDecCtasPerSm;
-    if (nCTA <= 0) return 0;
-    size_t a, b, c, d, e, f;
-    return dec_layout(cache, nCTA, &a, &b, &c, &d, &e, &f);
-}
-
-namespace csmkv {
 int decode_attn_check_args(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
                            const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
                            const void* out) {
@@ -827,7 +964,18 @@ int decode_attn_check_args(const void* q, const void* K, const void* V, const in
     if (cache->dtype == CSMKV_BF16 && (G > 8 || (D != 64 && D != 128))) return CSMKV_ERR_UNSUPPORTED;
     return CSMKV_OK;
 }
+
 }  // namespace csmkv
+
+using namespace csmkv;
+
+extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t h_q) {
+    if (check_cache(cache) != CSMKV_OK || h_q < 1 || (h_q % cache->h_kv) != 0) return 0;
+    const int nCTA = sm_count() * kDecCtasPerSm;
+    if (nCTA <= 0) return 0;
+    size_t a, b, c, d, e, f, g, h;
+    return dec_layout(cache, h_q, nCTA, &a, &b, &c, &d, &e, &f, &g, &h);
+}
 
 // Attention over the cache, optionally with the step's new token appended first
 // (k_new != NULL: bf16 fuses the append into the attention kernel).
@@ -841,8 +989,8 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     const bool bf16 = cache->dtype == CSMKV_BF16;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return CSMKV_ERR_CUDA;
-    size_t o_prefix, o_cta, o_cnt, o_pm, o_pl, o_pacc;
-    const size_t need = dec_layout(cache, nCTA, &o_prefix, &o_cta, &o_cnt, &o_pm, &o_pl, &o_pacc);
+    size_t o_first, o_n, o_sp, o_len, o_unit, o_pm, o_pl, o_pacc;
+    const size_t need = dec_layout(cache, h_q, nCTA, &o_first, &o_n, &o_sp, &o_len, &o_unit, &o_pm, &o_pl, &o_pacc);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -857,12 +1005,14 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     P.len_rw = const_cast<int32_t*>(len);
     P.out = out;
     P.hdr = reinterpret_cast<WsHeader*>(ws);
-    P.prefix = reinterpret_cast<int32_t*>(ws + o_prefix);
-    P.cta_unit = reinterpret_cast<int32_t*>(ws + o_cta);
+    P.g_first = reinterpret_cast<int32_t*>(ws + o_first);
+    P.g_n = reinterpret_cast<int32_t*>(ws + o_n);
+    P.g_sp = reinterpret_cast<int32_t*>(ws + o_sp);
+    P.g_len = reinterpret_cast<int32_t*>(ws + o_len);
+    P.g_unit = reinterpret_cast<int32_t*>(ws + o_unit);
     P.pm = reinterpret_cast<float*>(ws + o_pm);
     P.pl = reinterpret_cast<float*>(ws + o_pl);
     P.pacc = reinterpret_cast<float*>(ws + o_pacc);
-    P.counter = reinterpret_cast<int32_t*>(ws + o_cnt);
     P.BH = cache->batch * cache->h_kv;
     P.Hkv = cache->h_kv;
     P.Hq = h_q;
@@ -870,6 +1020,7 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     P.cap = cache->cap;
     P.D = D;
     P.nCTA = nCTA;
+    P.max_splits = dec_max_splits(nCTA, P.BH);
     P.scale = scale;
     P.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -904,7 +1055,9 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
                           CU_TENSOR_MAP_SWIZZLE_NONE))
             return CSMKV_ERR_CUDA;
     }
-    if (P.BH <= kMaxScanUnits)
+    // The in-CTA plan packs (len << kUnitBits) | unit into 32 bits.
+    const bool scan = P.BH <= kMaxScanUnits && cache->cap < (1 << (32 - kUnitBits));
+    if (scan)
         return D == 128 ? launch_decode_bf16<128, true>(P, tk, tv, tn, st) : launch_decode_bf16<64, true>(P, tk, tv, tn, st);
     decode_prologue_kernel<<<1, 1024, 0, st>>>(P);
     if (cudaGetLastError() != cudaSuccess) return CSMKV_ERR_CUDA;

@@ -41,10 +41,11 @@ struct WsHeader {
     int32_t epoch;        // call sequence number; flags equal to it are "set"
     int32_t levels_ch;    // CSM: max full chunks over active units
     int32_t levels_tail;  // CSM: max tail pieces over active units
-    int32_t total_tokens; // decode: tokens over all units
-    int32_t tokens_per_cta;
-    int32_t ctas_done;    // decode with append: CTAs finished; the last one bumps the lengths
-    int32_t pad[56];
+    int32_t dec_nsplits;  // decode (prologue path): token splits of the call
+    int32_t dec_split;    // decode (prologue path): base split length in tokens
+    int32_t ctas_done;    // decode: CTAs finished; the last one resets the ticket (and bumps lengths)
+    int32_t dec_total;    // decode (prologue path): rows attended over all units
+    int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 
