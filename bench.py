@@ -217,6 +217,52 @@ def oracle_sample(w, units=16, threads=None, decode=False):
     return res
 
 
+def near_tie_check(w, K0, V0, N0, L0, head_mask, p, units=16):
+    """The first round's merge decisions on a sample of units against the oracle: the
+    GPU compresses a copy of the sample's pristine caches (units are independent, so
+    its decisions are the ones the timed run makes), the oracle runs the same round on
+    the same stored values, and compare.check_round counts decisions that differ only
+    within the 1e-5 near-tie margin (allowed, logged) and any that differ beyond it
+    (failures). Part of the CPU-baseline leg: the oracle runs here only."""
+    import torch
+
+    import oracle
+    from oracle import compare
+    from online_kv_cache_chunked_gb300 import binding as B
+
+    rd = p.rounds[0]
+    if rd.step != 0:
+        return None
+    layers = max(1, min(w.layers, units // w.h_kv))  # whole layers of the first sequence's rows
+    rows = [l * w.seqs for l in range(layers)]  # batch index of (layer l, sequence 0)
+    K, V, N, L = (t[rows].clone() for t in (K0, V0, N0, L0))
+    hm = torch.from_numpy(np.asarray(head_mask, np.uint8)).cuda() if int(np.asarray(head_mask).sum()) else None
+    cache = B.cache_desc(K)
+    m = B.csm_edges_per_chunk(rd.r, w.c)
+    maxch = max(1, B.csm_max_chunks(cache, w.n1, w.n2, w.c))
+    BHs = K.shape[0] * K.shape[1]
+    match = torch.full((BHs, maxch, w.c // 2), -2, dtype=torch.int32, device="cuda")
+    ws = B.new_workspace(B.csm_workspace_bytes(cache, w.n1, w.n2, w.c))
+    pre_len = L.cpu().numpy().reshape(BHs)
+    top = int(pre_len.max())
+    preK = K[:, :, :top].cpu().to(torch.float64).numpy().reshape(BHs, top, w.d)
+    preV = V[:, :, :top].cpu().to(torch.float64).numpy().reshape(BHs, top, w.d)
+    preN = N[:, :, :top].cpu().numpy().reshape(BHs, top)
+    B.csm_compress_ex(K, V, N, L, w.n1, w.n2, w.c, rd.r, head_mask=hm, match_out=match, workspace=ws)
+    torch.cuda.synchronize()
+    gm = match.cpu().numpy()
+    skip = np.array([int(np.asarray(head_mask)[u % w.h_kv]) for u in range(BHs)], np.uint8)
+    free = oracle.csm_round(preK, preV, preN, pre_len, w.n1, w.n2, w.c, m, skip=skip)
+    n_chunks = np.array([0 if skip[u] else oracle.num_chunks(int(pre_len[u]), w.n1, w.n2, w.c) for u in range(BHs)])
+    log = []
+    dev, fails = compare.check_round(preK, free, gm, n_chunks, m, w.n1, w.c, log=log)
+    return {"units": int(BHs), "chunks": int(n_chunks.sum()), "deviating_chunks": int(dev),
+            "near_tie_decisions": len(log), "failures": len(fails), "records": log[:8],
+            "what": "first round's merge decisions (GPU) on the first sequence's caches of the first "
+                    f"{layers} layer(s) against the fp64 oracle on the same values; deviations allowed only "
+                    "within a 1e-5 similarity margin"}
+
+
 def dist_setup(n_gpus):
     import torch
     import torch.distributed as dist
@@ -429,6 +475,7 @@ def run_gpu(args):
     avg_launch_s = (attn_ms / 1e3) / max(1, attn_calls)
     csm_gbs = csm_bytes_step * args.steps / (csm_ms / 1e3) / 1e9
     cpu = oracle_sample(w, units=args.cpu_units, decode=True) if not args.no_cpu_baseline else None
+    near = near_tie_check(w, K0, V0, N0, L0, head_mask, p) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC,
         "value": agg["tokens"] / agg["csm_s"],
@@ -468,6 +515,8 @@ def run_gpu(args):
                                                           + (1 if flush is not None else 0)) * w.steps),
         "clocks": clocks,
     }
+    if near is not None:
+        line["near_ties"] = near
     if cpu is not None:
         line["cpu_baseline"] = {"value": cpu["value"], "unit": "tokens/s", "cores": cpu["cores"], "kind": "oracle",
                                 "sample": cpu["sample"], "seconds": cpu["seconds"], "decode": cpu.get("decode")}

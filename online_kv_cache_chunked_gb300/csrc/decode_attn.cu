@@ -62,11 +62,11 @@ constexpr int kSlotHeads = 8;          // query heads of a group the MMA covers 
 // Base split length for `total` tokens on n CTAs: about kItemsPerCta splits per
 // CTA, a multiple of the tile, at least kMinSplit. Since S >= total / (n *
 // kItemsPerCta), a call has at most n * kItemsPerCta + units splits.
-__host__ __device__ __forceinline__ int split_base(long long total, int n) {
-    const long long per = (long long)n * kItemsPerCta;
-    long long s = (total + per - 1) / per;
-    s = (s + kTile - 1) / kTile * kTile;
-    return (int)(s > kMinSplit ? s : kMinSplit);
+__host__ __device__ __forceinline__ int split_base(int total, int n) {
+    const unsigned per = (unsigned)n * kItemsPerCta;
+    unsigned s = ((unsigned)total + per - 1u) / per;
+    s = (s + kTile - 1u) / kTile * kTile;
+    return (int)(s > (unsigned)kMinSplit ? s : (unsigned)kMinSplit);
 }
 // Split length of a unit of `len` rows (of `total` over n CTAs): the base S, or
 // longer for a long unit, so that it has at most kMaxSplitsPerUnit splits -- or,
@@ -87,6 +87,7 @@ __device__ __forceinline__ int unit_class(int n, int su, int S) {
     return su > S ? 0 : (n >= 16 ? 1 : (n >= 4 ? 2 : 3));
 }
 
+// At most total / S <= nCTA * kItemsPerCta splits plus one per unit.
 __host__ __device__ __forceinline__ int dec_max_splits(int nCTA, int BH) { return nCTA * kItemsPerCta + BH; }
 
 struct DecParams {
@@ -104,7 +105,6 @@ struct DecParams {
     WsHeader* hdr;
     int32_t* g_first;     // [BH] first split of every unit (written by the plan)
     int32_t* g_n;         // [BH] splits of every unit
-    int32_t* g_sp;        // prologue path: [BH + 1] first split of every unit
     int32_t* g_len;       // prologue path: [BH] rows attended per unit
     int32_t* g_unit;      // prologue path: [max splits] unit of every split
     float* pm;            // [splits][G] running max (base-2 domain)
@@ -167,7 +167,7 @@ __device__ __forceinline__ void block_scan8(int (&v)[8], int (&tot)[8], int (*sc
 __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p) {
     griddep_launch_dependents();  // the main kernel may set itself up meanwhile
     __shared__ int scratch[32][8];
-    __shared__ int carry_s;
+    __shared__ int carry_s[2];
     const int tid = threadIdx.x;
     long long total = 0;
     for (int base = 0; base < p.BH; base += 1024) {
@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p
         block_scan8(v, t, scratch);
         total += t[0];
     }
-    const int S = split_base(total, p.nCTA);
+    const int S = split_base((int)total, p.nCTA);
     if (tid == 0) {
-        carry_s = 0;
+        carry_s[1] = 0;
         p.hdr->dec_total = (int32_t)total;
     }
     const int total32 = (int)total;
@@ -188,22 +188,20 @@ __global__ void __launch_bounds__(1024) decode_prologue_kernel(const DecParams p
         const int u = base + tid;
         const int len = u < p.BH ? p.g_len[u] : 0;
         const int n = len > 0 ? unit_nsplit(len, unit_split(len, S, total32, p.nCTA)) : 0;
-        int v[8] = {n, 0, 0, 0, 0, 0, 0, 0}, t[8];
-        block_scan8(v, t, scratch);
-        const int first = carry_s + v[0];
+        int w[8] = {n, 0, 0, 0, 0, 0, 0, 0}, t2[8];
+        block_scan8(w, t2, scratch);
+        const int first = carry_s[1] + w[0];
         if (u < p.BH) {
-            p.g_sp[u] = first;
             p.g_first[u] = first;
             p.g_n[u] = n;
             for (int k = 0; k < n; ++k) p.g_unit[first + k] = u;
         }
         __syncthreads();
-        if (tid == 0) carry_s += t[0];
+        if (tid == 0) carry_s[1] += t2[0];
         __syncthreads();
     }
     if (tid == 0) {
-        p.g_sp[p.BH] = carry_s;
-        p.hdr->dec_nsplits = carry_s;
+        p.hdr->dec_nsplits = carry_s[1];
         p.hdr->dec_split = S;
     }
 }
@@ -263,6 +261,7 @@ struct DecSmall {
 // One split, resolved from its ticket.
 struct Split {
     int t, u, k, n, len, su;
+    int tok0, ntok;  // the split's rows within the unit
 };
 
 __device__ __forceinline__ void consumer_barrier() {
@@ -285,17 +284,17 @@ __device__ __forceinline__ bool consumer_any(bool v) {
 }
 
 // Ticket -> split. SCAN: the CTA's own tables (positions in ticket order: sp =
-// first split, ulen = len << kUnitBits | unit); otherwise the prologue's
-// global tables (units in index order, g_unit maps a split to its unit).
+// first split, ulen = len << kUnitBits | unit); otherwise the prologue's global
+// tables (units in index order, g_unit maps a split to its unit).
 template <bool SCAN>
 __device__ __forceinline__ Split resolve_split(const DecParams& p, int t, int nsplits, int S, int total,
                                                const int* sp, const uint32_t* ulen) {
     Split r;
     r.t = -1;
     if (t < 0 || t >= nsplits) return r;
-    int first, last1;
+    int first;
     if constexpr (SCAN) {
-        int lo = 0, hi = p.BH;  // last position with sp[pos] <= t
+        int lo = 0, hi = p.BH;  // last position with first split <= t
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (sp[mid] <= t) lo = mid; else hi = mid;
@@ -304,17 +303,18 @@ __device__ __forceinline__ Split resolve_split(const DecParams& p, int t, int ns
         r.u = (int)(x & ((1u << kUnitBits) - 1u));
         r.len = (int)(x >> kUnitBits);
         first = sp[lo];
-        last1 = sp[lo + 1];
+        r.n = sp[lo + 1] - first;
     } else {
         r.u = __ldcg(p.g_unit + t);
         r.len = __ldcg(p.g_len + r.u);
-        first = __ldcg(p.g_sp + r.u);
-        last1 = __ldcg(p.g_sp + r.u + 1);
+        first = __ldcg(p.g_first + r.u);
+        r.n = __ldcg(p.g_n + r.u);
     }
     r.t = t;
     r.k = t - first;
-    r.n = last1 - first;
     r.su = unit_split(r.len, S, total, p.nCTA);
+    r.tok0 = r.k * r.su;
+    r.ntok = min(r.su, r.len - r.tok0);
     return r;
 }
 
@@ -418,6 +418,29 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecP
     }
 }
 
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// Exclusive prefix sum over the warp's lanes.
+__device__ __forceinline__ int warp_excl(int v) {
+    const int lane = threadIdx.x & 31;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    return incl - v;
+}
+// Ticket-order class of a unit of `len` rows (empty units last).
+__device__ __forceinline__ int plan_class(int len, int S, int total, int n) {
+    if (len <= 0) return 3;
+    const int su = unit_split(len, S, total, n);
+    return unit_class(unit_nsplit(len, su), su, S);
+}
+
 // SCAN: the CTA computes the unit order and split offsets itself (units <=
 // kMaxScanUnits, kept in shared memory); otherwise decode_prologue_kernel has
 // written them to the workspace.
@@ -458,86 +481,67 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
     // ---------------------------------------------------------------- split plan
     if constexpr (SCAN) {
-        // One warp plans the call with shuffles only: every lane holds the rows of
-        // up to kPer consecutive units (all loads in flight at once).
+        // Every thread loads some units' rows into sp[] (indexed by unit for now);
+        // then one warp plans the call with rolled loops and shuffles. The code is
+        // kept short on purpose: a call streams more than L2 holds, so this code is
+        // fetched cold on every call.
+#pragma unroll 4
+        for (int u = tid; u < p.BH; u += kDecThreads) sp[u] = eff_len(p, u, true);
+        __syncthreads();
         if (warp == 0) {
-            constexpr int kPer = kMaxScanUnits / 32;
             const int per = (p.BH + 31) / 32;
-            const int ub = lane * per;
-            int lr[kPer];
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) lr[i] = (i < per && ub + i < p.BH) ? eff_len(p, ub + i, true) : 0;
+            const int ub = min(p.BH, lane * per), ue = min(p.BH, ub + per);
             int total = 0;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) total += lr[i];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+#pragma unroll 1
+            for (int u = ub; u < ue; ++u) total += sp[u];
+            total = warp_sum(total);
             const int S = split_base(total, (int)gridDim.x);
-            // units and splits per class, then positions: classes in order, units in
-            // index order inside a class
-            int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                if (i < per && ub + i < p.BH) {
-                    const int len = lr[i];
-                    const int su = len > 0 ? unit_split(len, S, total, p.nCTA) : S;
-                    const int n = len > 0 ? unit_nsplit(len, su) : 0;
-                    const int cls = n > 0 ? unit_class(n, su, S) : 3;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (k == cls) {
-                            c[k] += 1;
-                            c[4 + k] += n;
-                        }
-                    }
-                }
+            // positions: classes in order, units in index order inside a class; the
+            // four class counts (each <= kMaxScanUnits < 2^16) travel packed in two ints
+            int c01 = 0, c23 = 0;
+#pragma unroll 1
+            for (int u = ub; u < ue; ++u) {
+                const int cls = plan_class(sp[u], S, total, p.nCTA);
+                c01 += cls == 0 ? 1 : (cls == 1 ? 0x10000 : 0);
+                c23 += cls == 2 ? 1 : (cls == 3 ? 0x10000 : 0);
             }
-            int upos[4], spos[4], ru = 0, rs = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int incl = c[k];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += x;
-                }
-                const int tot = __shfl_sync(0xffffffffu, incl, 31);
-                if (k < 4) {
-                    upos[k] = ru + incl - c[k];
-                    ru += tot;
-                } else {
-                    spos[k - 4] = rs + incl - c[k];
-                    rs += tot;
-                }
+            const int e01 = warp_excl(c01), e23 = warp_excl(c23);
+            const int t01 = __shfl_sync(0xffffffffu, e01 + c01, 31), t23 = __shfl_sync(0xffffffffu, e23 + c23, 31);
+            int pos0 = e01 & 0xFFFF;
+            int pos1 = (t01 & 0xFFFF) + (e01 >> 16);
+            int pos2 = (t01 & 0xFFFF) + (t01 >> 16) + (e23 & 0xFFFF);
+            int pos3 = (t01 & 0xFFFF) + (t01 >> 16) + (t23 & 0xFFFF) + (e23 >> 16);
+#pragma unroll 1
+            for (int u = ub; u < ue; ++u) {
+                const int cls = plan_class(sp[u], S, total, p.nCTA);
+                const int pos = cls == 0 ? pos0++ : (cls == 1 ? pos1++ : (cls == 2 ? pos2++ : pos3++));
+                ulen[pos] = ((uint32_t)sp[u] << kUnitBits) | (uint32_t)u;
             }
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const int u = ub + i;
-                if (i < per && u < p.BH) {
-                    const int len = lr[i];
-                    const int su = len > 0 ? unit_split(len, S, total, p.nCTA) : S;
-                    const int n = len > 0 ? unit_nsplit(len, su) : 0;
-                    const int cls = n > 0 ? unit_class(n, su, S) : 3;
-                    int pos = 0, first = 0;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (k == cls) {
-                            pos = upos[k]++;
-                            first = spos[k];
-                            spos[k] += n;
-                        }
-                    }
-                    sp[pos] = first;
-                    ulen[pos] = ((uint32_t)len << kUnitBits) | (uint32_t)u;
-                    if (blockIdx.x == 0) {  // for the merge kernel
-                        p.g_first[u] = first;
-                        p.g_n[u] = n;
-                    }
+            __syncwarp();
+            // in ticket order: every position's splits and its first split
+            int ns = 0;
+#pragma unroll 1
+            for (int q = ub; q < ue; ++q) {
+                const int len = (int)(ulen[q] >> kUnitBits);
+                ns += len > 0 ? unit_nsplit(len, unit_split(len, S, total, p.nCTA)) : 0;
+            }
+            int first = warp_excl(ns);
+            const int nsplits_all = __shfl_sync(0xffffffffu, first + ns, 31);
+#pragma unroll 1
+            for (int q = ub; q < ue; ++q) {
+                const int len = (int)(ulen[q] >> kUnitBits);
+                const int n = len > 0 ? unit_nsplit(len, unit_split(len, S, total, p.nCTA)) : 0;
+                sp[q] = first;
+                if (blockIdx.x == 0) {  // for the merge kernel
+                    const int u = (int)(ulen[q] & ((1u << kUnitBits) - 1u));
+                    p.g_first[u] = first;
+                    p.g_n[u] = n;
                 }
+                first += n;
             }
             if (lane == 0) {
-                sp[p.BH] = rs;
-                sm.nsplits = rs;
+                sp[p.BH] = nsplits_all;
+                sm.nsplits = nsplits_all;
                 sm.S = S;
                 sm.total = total;
             }
@@ -556,12 +560,15 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         // ============================================================ producer
         int issued = 0;
         bool ok = true;
+        // K and V are read once per call: their lines go first when L2 needs room, so the
+        // kernel's code, the lengths, q and the split records stay resident
+        const uint64_t pol = l2_policy_evict_first();
         // split blockIdx.x first; later splits come from the ticket, from gridDim.x on
         Split cur = resolve_split<SCAN>(p, (int)blockIdx.x, nsplits, S, total, sp, ulen);
         while (cur.t >= 0) {
             int tn = 0;
-            const int tok0 = cur.k * cur.su;
-            const int ntok = min(cur.su, cur.len - tok0);
+            const int tok0 = cur.tok0;
+            const int ntok = cur.ntok;
             const int ntiles = (ntok + kTile - 1) / kTile;
             const long long row_base = (long long)cur.u * p.cap;
             int arow = -1;  // fused append: the unit's new row, held by its last split
@@ -628,8 +635,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                     }
 #pragma unroll
                     for (int bx = 0; bx < Geo::kBoxes; ++bx) {
-                        tma_load_2d(st + Geo::kKOff + bx * Geo::kBoxBytes, &tmK, &full[s], bx * 64, row);
-                        tma_load_2d(st + Geo::kVOff + bx * Geo::kBoxBytes, &tmV, &full[s], bx * 64, row);
+                        tma_load_2d_hint(st + Geo::kKOff + bx * Geo::kBoxBytes, &tmK, &full[s], bx * 64, row, pol);
+                        tma_load_2d_hint(st + Geo::kVOff + bx * Geo::kBoxBytes, &tmV, &full[s], bx * 64, row, pol);
                     }
                     tma_load_2d(nbase + s * Geo::kNStride, &tmN, &full[s], 0, row >> 2);
                 }
@@ -906,7 +913,7 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const DecParams p, cons
     }
 }
 
-static size_t dec_layout(const csmkv_cache* cache, int32_t h_q, int nCTA, size_t* o_first, size_t* o_n, size_t* o_sp,
+static size_t dec_layout(const csmkv_cache* cache, int32_t h_q, int nCTA, size_t* o_first, size_t* o_n,
                          size_t* o_len, size_t* o_unit, size_t* o_pm, size_t* o_pl, size_t* o_pacc) {
     const size_t BH = (size_t)cache->batch * cache->h_kv;
     const size_t G = (size_t)h_q / cache->h_kv;
@@ -916,8 +923,6 @@ static size_t dec_layout(const csmkv_cache* cache, int32_t h_q, int nCTA, size_t
     off = align_up(off + BH * 4, 256);
     *o_n = off;
     off = align_up(off + BH * 4, 256);
-    *o_sp = off;
-    off = align_up(off + (BH + 1) * 4, 256);
     *o_len = off;
     off = align_up(off + BH * 4, 256);
     *o_unit = off;
@@ -973,8 +978,8 @@ extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t 
     if (check_cache(cache) != CSMKV_OK || h_q < 1 || (h_q % cache->h_kv) != 0) return 0;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return 0;
-    size_t a, b, c, d, e, f, g, h;
-    return dec_layout(cache, h_q, nCTA, &a, &b, &c, &d, &e, &f, &g, &h);
+    size_t a, b, c, d, e, f, g;
+    return dec_layout(cache, h_q, nCTA, &a, &b, &c, &d, &e, &f, &g);
 }
 
 // Attention over the cache, optionally with the step's new token appended first
@@ -989,8 +994,8 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     const bool bf16 = cache->dtype == CSMKV_BF16;
     const int nCTA = sm_count() * kDecCtasPerSm;
     if (nCTA <= 0) return CSMKV_ERR_CUDA;
-    size_t o_first, o_n, o_sp, o_len, o_unit, o_pm, o_pl, o_pacc;
-    const size_t need = dec_layout(cache, h_q, nCTA, &o_first, &o_n, &o_sp, &o_len, &o_unit, &o_pm, &o_pl, &o_pacc);
+    size_t o_first, o_n, o_len, o_unit, o_pm, o_pl, o_pacc;
+    const size_t need = dec_layout(cache, h_q, nCTA, &o_first, &o_n, &o_len, &o_unit, &o_pm, &o_pl, &o_pacc);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1007,7 +1012,6 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     P.hdr = reinterpret_cast<WsHeader*>(ws);
     P.g_first = reinterpret_cast<int32_t*>(ws + o_first);
     P.g_n = reinterpret_cast<int32_t*>(ws + o_n);
-    P.g_sp = reinterpret_cast<int32_t*>(ws + o_sp);
     P.g_len = reinterpret_cast<int32_t*>(ws + o_len);
     P.g_unit = reinterpret_cast<int32_t*>(ws + o_unit);
     P.pm = reinterpret_cast<float*>(ws + o_pm);
