@@ -331,6 +331,8 @@ def workload_of(args):
     from online_kv_cache_chunked_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
+    if getattr(args, "layers", None):  # a smaller or larger stack of the same layer shape
+        w = synth.scaled(w, layers=int(args.layers), name=f"{w.name}[{int(args.layers)} layers]")
     return synth.scaled(w, budget_exact=True) if getattr(args, "budget_exact", False) else w
 
 
@@ -374,7 +376,12 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     d = synth.make_device(w)
     K0, V0, N0, L0 = (d[k].clone() for k in ("K", "V", "N", "len"))
-    p = Pipeline(w, d, stream=None, csm_kernel=CSM_KERNELS[args.csm_kernel])
+    kv = None
+    if args.paged:  # the same cache in pages of args.page_rows rows scattered over one pool per array
+        from online_kv_cache_chunked_gb300 import paged as PG
+        kv = PG.to_paged(d["K"], d["V"], d["N"], args.page_rows, spare_pages=64, seed=w.seed)
+        kv0 = tuple(t.clone() for t in (kv.K, kv.V, kv.N))
+    p = Pipeline(w, d, stream=None, csm_kernel=CSM_KERNELS[args.csm_kernel], paged=kv)
     head_mask = d["head_mask"].cpu().numpy()
     rounds = p.rounds
 
@@ -418,7 +425,9 @@ def run_gpu(args):
         pre_marks.append(e)
 
     def one_step(timed):
-        for dst, src in ((d["K"], K0), (d["V"], V0), (d["N"], N0), (d["len"], L0)):
+        pairs = ((kv.K, kv0[0]), (kv.V, kv0[1]), (kv.N, kv0[2])) if kv is not None else (
+            (d["K"], K0), (d["V"], V0), (d["N"], N0))
+        for dst, src in pairs + ((d["len"], L0),):
             dst.copy_(src, non_blocking=True)
         pre_marks.clear()
         p.run_native(hook=hook if timed else None, attn_events=ev_att if timed else None,
@@ -465,7 +474,12 @@ def run_gpu(args):
     agg = aggregate(local_res, world)
 
     # ---- end to end through the C ABI from pinned host buffers
-    e2e = e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args) if rank == 0 else None
+    if rank != 0:
+        e2e = None
+    elif kv is not None:
+        e2e = e2e_measure_paged(w, d, kv, kv0, L0, p, rounds, args)
+    else:
+        e2e = e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args)
     clocks = clk.summary()
     if rank != 0:
         return 0
@@ -491,16 +505,18 @@ def run_gpu(args):
         "data": "synthetic (seeded AR(1) keys, N(0,1) values, N(0,I) queries; no model weights)",
         "config": dict(config_of(w, world), l2=("a 2xL2 buffer is read before every attention call" if flush is not None
                                           else "every attention call reads more than 2xL2 of cache"),
-                       csm_kernel=args.csm_kernel),
+                       csm_kernel=args.csm_kernel,
+                       layout=(f"paged: {args.page_rows}-row pages scattered over a pool (block table per "
+                               "(sequence, KV head))" if kv is not None else "dense")),
         "decode_attn": {"value": attn_gbs, "unit": "GB/s", "frac_of_measured_peak": attn_gbs / hbm,
                         "frac_of_nominal_7900": attn_gbs / 7900.0, "calls_timed": attn_calls,
                         "avg_call_us": 1e6 * avg_launch_s},
         "roofline": {"bound": "hbm", "achieved": per_launch_bytes / avg_launch_s / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": per_launch_bytes / avg_launch_s / 1e9 / hbm,
-                     "traffic": traffic_record("decode_attn", "bytes_per_launch", w), "kernel": "decode_step_logn (append + log-N attention, one kernel)",
+                     "traffic": traffic_record("decode_attn", "bytes_per_launch", w) if kv is None else None, "kernel": "decode_step_logn (append + log-N attention, one kernel)",
                      "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
         "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
-                         "traffic": traffic_record("csm_compress", "bytes_per_step", w), "kernel": "csm_compress",
+                         "traffic": traffic_record("csm_compress", "bytes_per_step", w) if kv is None else None, "kernel": "csm_compress",
                          "csm_kernel": args.csm_kernel,
                          "peak_kind": kind, "bytes_per_step": csm_bytes_step},
         "csm": {"tokens_per_step": csm_tokens_step, "head_tokens_per_s": agg["tokens"] * (w.h_kv - int(head_mask.sum())) / agg["csm_s"],
@@ -522,6 +538,39 @@ def run_gpu(args):
                                 "sample": cpu["sample"], "seconds": cpu["seconds"], "decode": cpu.get("decode")}
     print(json.dumps(line))
     return 0
+
+
+def e2e_measure_paged(w, d, kv, kv0, L0, p, rounds, args):
+    """The paged layout end to end: H2D of the pools and the lengths from pinned host
+    buffers, the prefill round(s) through the paged entry point, D2H of the pools."""
+    import torch
+
+    from online_kv_cache_chunked_gb300 import binding as B
+
+    host = [t.cpu().pin_memory() for t in kv0] + [L0.cpu().pin_memory()]
+    back = [torch.empty_like(t, device="cpu").pin_memory() for t in (kv.K, kv.V, kv.N)]
+    dev = [kv.K, kv.V, kv.N, d["len"]]
+    stream = torch.cuda.current_stream()
+    pre_k = [k for k, rd in enumerate(rounds) if rd.step == 0]
+    tokens = sum(csm_call_stats(w, rounds[k], d["head_mask"].cpu().numpy())[0] for k in pre_k)
+    times = []
+    for it in range(args.warmup + max(1, args.steps)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for dst, src in zip(dev, host):
+            dst.copy_(src, non_blocking=True)
+        p.compress_at(0)
+        for dst, src in zip(back, (kv.K, kv.V, kv.N)):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in back)
+    return {"value": tokens / float(np.median(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "what": "paged layout: H2D of the pools, the prefill round(s) "
+            "through the paged entry point, D2H of the pools (one stream, not pipelined)"}
 
 
 def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
@@ -635,8 +684,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
                     help="zero a 2xL2 buffer before every attention call (auto: when a call reads < 2xL2)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run the workload with this many layers (e.g. a small stack for profiling captures)")
     ap.add_argument("--budget-exact", action="store_true",
                     help="each round merges only the oldest chunks needed to bring s under the budget")
+    ap.add_argument("--paged", action="store_true",
+                    help="run on a paged (block-table) copy of the cache: pages of --page-rows rows at scattered "
+                         "pool pages")
+    ap.add_argument("--page-rows", type=int, default=256)
     ap.add_argument("--shard", default="weak", choices=["weak", "strong"],
                     help="with N ranks: weak = N copies of the workload's shape, one per rank (per-GPU work "
                          "fixed); strong = the workload's own units split over the ranks")

@@ -244,6 +244,54 @@ int decode_attn_logn_noalloc(const void* q, const void* K, const void* V, const 
                              void* out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Paged (block-table) cache layout   [CentroidKV 技术摘要, 结果: the method
+ *                                     serving inside vLLM's paged KV cache]
+ *
+ * Pages of page_rows rows are taken from one pool per array: K and V are
+ * [num_pages][page_rows][head_dim] in the cache dtype, N is int32
+ * [num_pages][page_rows]. Every (sequence, KV head) unit u owns the pages its
+ * block table lists: logical row r of unit u lives in pool row
+ *     table[u * max_pages + r / page_rows] * page_rows + r % page_rows.
+ * The csmkv_cache descriptor describes the logical cache as for the dense
+ * layout, with cap = max_pages * page_rows; len stays [batch][h_kv]. A page
+ * may belong to at most one (unit, logical page): compression compacts every
+ * unit in place through its own pages. Pages past a unit's rows need not be
+ * listed (any value); a listed page that the call touches must be in
+ * [0, num_pages): an access through an entry outside it is skipped and
+ * CSMKV_ERR_ARG recorded in the workspace status word.
+ * page_rows: a multiple of 64, >= 64. Pools 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    const int32_t* table; /* device int32 [batch * h_kv][max_pages] */
+    int32_t page_rows;
+    int32_t max_pages;
+    int32_t num_pages;    /* pages in each pool */
+} csmkv_pages;
+
+/* csm_append on a paged cache (any dtype). */
+int csm_append_paged(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache, const csmkv_pages* pages,
+                     const void* k_new, const void* v_new, const uint8_t* seq_mask, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/* csm_compress_ex on a paged cache: the same round, decisions and results (bit
+ * for bit, given the same decisions) as on the dense layout. Tensor-core shapes
+ * only (bf16, c == 256, head_dim in {64, 128}; CSMKV_ERR_UNSUPPORTED
+ * otherwise); workspace as csm_workspace_bytes(cache, ...) with the logical
+ * cap. match_out and opts as for csm_compress_ex (opts->kernel is ignored). */
+int csm_compress_paged(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache, const csmkv_pages* pages,
+                       int32_t n1, int32_t n2, int32_t c, double r, const uint8_t* head_mask, const uint8_t* seq_mask,
+                       int32_t* match_out, const csm_options* opts, void* workspace, size_t ws_bytes, void* stream);
+
+/* decode_attn_logn / decode_step_logn on a paged cache (bf16 only;
+ * CSMKV_ERR_UNSUPPORTED otherwise); workspace as decode_attn_workspace_bytes. */
+int decode_attn_logn_paged(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
+                           const csmkv_cache* cache, const csmkv_pages* pages, int32_t h_q, float scale, void* out,
+                           void* workspace, size_t ws_bytes, void* stream);
+int decode_step_logn_paged(const void* q, const void* k_new, const void* v_new, void* K, void* V, int32_t* N,
+                           int32_t* len, const csmkv_cache* cache, const csmkv_pages* pages, int32_t h_q, float scale,
+                           void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * The decode loop, issued natively   [Chelsea §三 算法流程, Algorithm 1
  *                                     (decode phase); CentroidKV 技术摘要:
  *                                     推理流水线]
@@ -320,6 +368,8 @@ typedef struct {
     size_t l2_flush_bytes;
     int32_t fused_append; /* nonzero: each step's append and attention run as one
                              decode_step_logn (ws_append unused) */
+    const csmkv_pages* pages; /* NULL: dense layout; else every call uses the paged
+                             entry points (fused_append must then be nonzero) */
 } csm_decode_loop;
 
 int csm_decode_run(const csm_decode_loop* loop, int32_t first_step, int32_t steps, void* stream);

@@ -46,6 +46,34 @@ class CsmRoundPlan(ctypes.Structure):
                 ("seq_max_chunks", ctypes.c_void_p)]
 
 
+class Pages(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("page_rows", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
+
+
+class PagedKV:
+    """A paged (block-table) cache as the C ABI sees it: pools K, V [num_pages, page_rows,
+    head_dim] (cache dtype) and N [num_pages, page_rows] (int32), a block table
+    [batch * h_kv, max_pages] (int32, device), and the logical shape it stands for
+    (batch, h_kv, cap = max_pages * page_rows)."""
+
+    def __init__(self, K, V, N, table, batch, h_kv):
+        self.K, self.V, self.N, self.table = K, V, N, table
+        self.batch, self.h_kv = int(batch), int(h_kv)
+        self.num_pages, self.page_rows, self.head_dim = (int(x) for x in K.shape)
+        self.max_pages = int(table.shape[1])
+
+    @property
+    def cap(self):
+        return self.max_pages * self.page_rows
+
+    def cache(self) -> "Cache":
+        return Cache(self.batch, self.h_kv, self.head_dim, self.cap, _DTYPES[self.K.dtype])
+
+    def pages(self) -> Pages:
+        return Pages(self.table.data_ptr(), self.page_rows, self.max_pages, self.num_pages)
+
+
 class CsmDecodeLoop(ctypes.Structure):
     _fields_ = [("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("N", ctypes.c_void_p), ("len", ctypes.c_void_p),
                 ("cache", Cache), ("h_q", ctypes.c_int32), ("scale", ctypes.c_float),
@@ -58,7 +86,7 @@ class CsmDecodeLoop(ctypes.Structure):
                 ("ws_attn", ctypes.c_void_p), ("ws_attn_bytes", ctypes.c_size_t),
                 ("attn_events", ctypes.POINTER(ctypes.c_void_p)), ("csm_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("l2_flush", ctypes.c_void_p), ("l2_flush_bytes", ctypes.c_size_t),
-                ("fused_append", ctypes.c_int32)]
+                ("fused_append", ctypes.c_int32), ("pages", ctypes.POINTER(Pages))]
 
 
 _lib = None
@@ -83,6 +111,13 @@ _SIGS = {
     "decode_attn_logn_noalloc": (ctypes.c_int, [P, P, P, P, P, CP, I32, ctypes.c_float, P, P]),
     "decode_step_logn": (ctypes.c_int, [P, P, P, P, P, P, P, CP, I32, ctypes.c_float, P, P, SZ, P]),
     "csm_decode_run": (ctypes.c_int, [ctypes.POINTER(CsmDecodeLoop), I32, I32, P]),
+    "csm_append_paged": (ctypes.c_int, [P, P, P, P, CP, ctypes.POINTER(Pages), P, P, P, P, SZ, P]),
+    "csm_compress_paged": (ctypes.c_int, [P, P, P, P, CP, ctypes.POINTER(Pages), I32, I32, I32, F64, P, P, P,
+                                          ctypes.POINTER(CsmOptions), P, SZ, P]),
+    "decode_attn_logn_paged": (ctypes.c_int, [P, P, P, P, P, CP, ctypes.POINTER(Pages), I32, ctypes.c_float, P,
+                                              P, SZ, P]),
+    "decode_step_logn_paged": (ctypes.c_int, [P, P, P, P, P, P, P, CP, ctypes.POINTER(Pages), I32,
+                                              ctypes.c_float, P, P, SZ, P]),
     "csm_budget": (F64, [I64, F64, I64]),
     "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
     "csm_ratio": (F64, [I32, F64, F64, F64]),
@@ -248,13 +283,15 @@ def _event_array(events):
 
 def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), head_mask=None,
                    ws_csm=None, ws_append=None, ws_attn=None, first_step=1, steps=None, csm_kernel=0,
-                   attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None, fused_append=False):
+                   attn_events=None, csm_events=None, l2_flush=None, scale=None, stream=None, fused_append=False,
+                   paged=None):
     """Decode steps first_step .. first_step+steps-1 (1-based) issued natively: per step
     append(k_new[i-1], v_new[i-1]), attention(q[i-1]) -> out[i-1], then the planned
     rounds of that step. rounds: iterable of (step, r, seq_mask or None[, seq_max_chunks or
     None]), sorted by step.
-    attn_events / csm_events: torch.cuda.Event lists (2 per call), recorded once before."""
-    cache = cache_desc(K)
+    attn_events / csm_events: torch.cuda.Event lists (2 per call), recorded once before.
+    paged: a PagedKV (K, V, N are then its pools; every call uses the paged entry points)."""
+    cache = paged.cache() if paged is not None else cache_desc(K)
     if steps is None:
         steps = q.shape[0] - first_step + 1
     if scale is None:
@@ -271,8 +308,51 @@ def csm_decode_run(K, V, N, length, q, k_new, v_new, out, n1, n2, c, rounds=(), 
                          _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), int(n1), int(n2), int(c), _ptr(head_mask),
                          int(csm_kernel), rarr, len(rl), _ptr(ws_csm), nb(ws_csm), _ptr(ws_append), nb(ws_append),
                          _ptr(ws_attn), nb(ws_attn), ae, ce, _ptr(l2_flush), nb(l2_flush), int(bool(fused_append)))
+    pg = paged.pages() if paged is not None else None
+    if pg is not None:
+        loop.pages = ctypes.pointer(pg)
     rc = load().csm_decode_run(ctypes.byref(loop), int(first_step), int(steps), _stream(stream))
     _check("csm_decode_run", rc)
+
+
+# ---------------------------------------------------------------- paged layout
+def csm_append_paged(kv, length, k_new, v_new, seq_mask=None, workspace=None, stream=None):
+    cache, pg = kv.cache(), kv.pages()
+    rc = load().csm_append_paged(_ptr(kv.K), _ptr(kv.V), _ptr(kv.N), _ptr(length), ctypes.byref(cache),
+                                 ctypes.byref(pg), _ptr(k_new), _ptr(v_new), _ptr(seq_mask), _ptr(workspace),
+                                 workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("csm_append_paged", rc)
+
+
+def csm_compress_paged(kv, length, n1, n2, c, r, head_mask=None, seq_mask=None, match_out=None, wait_timeout_ns=0,
+                       seq_max_chunks=None, workspace=None, stream=None):
+    cache, pg = kv.cache(), kv.pages()
+    opts = CsmOptions(int(wait_timeout_ns), 0, 0, _ptr(seq_max_chunks))
+    rc = load().csm_compress_paged(_ptr(kv.K), _ptr(kv.V), _ptr(kv.N), _ptr(length), ctypes.byref(cache),
+                                   ctypes.byref(pg), n1, n2, c, float(r), _ptr(head_mask), _ptr(seq_mask),
+                                   _ptr(match_out), ctypes.byref(opts), _ptr(workspace),
+                                   workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("csm_compress_paged", rc)
+
+
+def decode_attn_logn_paged(q, kv, length, out, workspace, scale=None, stream=None):
+    cache, pg = kv.cache(), kv.pages()
+    if scale is None:
+        scale = 1.0 / (kv.head_dim ** 0.5)
+    rc = load().decode_attn_logn_paged(_ptr(q), _ptr(kv.K), _ptr(kv.V), _ptr(kv.N), _ptr(length),
+                                       ctypes.byref(cache), ctypes.byref(pg), q.shape[1], float(scale), _ptr(out),
+                                       _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("decode_attn_logn_paged", rc)
+
+
+def decode_step_logn_paged(q, k_new, v_new, kv, length, out, workspace, scale=None, stream=None):
+    cache, pg = kv.cache(), kv.pages()
+    if scale is None:
+        scale = 1.0 / (kv.head_dim ** 0.5)
+    rc = load().decode_step_logn_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv.K), _ptr(kv.V), _ptr(kv.N),
+                                       _ptr(length), ctypes.byref(cache), ctypes.byref(pg), q.shape[1], float(scale),
+                                       _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("decode_step_logn_paged", rc)
 
 
 # ---------------------------------------------------------------- host helpers

@@ -31,6 +31,7 @@ struct CsmParams {
     const uint8_t* head_mask;
     const uint8_t* seq_mask;
     const int32_t* seq_limit;  // [batch] or NULL: at most this many chunks of sequence b (<= 0: all)
+    RowMap rm;                 // logical row -> pool row (a paged layout's block table)
     int32_t BH, h_kv, cap, D, n1, n2, c, m, maxch, L;
     int64_t timeout_ns;
     int32_t withhold;
@@ -283,7 +284,9 @@ __device__ __forceinline__ void chunk_deps(int j, int c, int m, int& lo, int& hi
 
 // One tail piece: up to 64 rows of the remainder + recent window moved down by
 // ch*m rows, staged through `stage` (>= 2 * 64 * row bytes), degrees through sN.
-template <typename T>
+// PAGED: every row goes through the block table (rows whose entry is outside the
+// pool are skipped and CSMKV_ERR_ARG recorded).
+template <typename T, bool PAGED = false>
 __device__ bool tail_piece(const CsmParams& p, int u, int piece, int32_t epoch, uint8_t* stage, int32_t* sN) {
     const int tid = threadIdx.x;
     const int c = p.c, m = p.m, D = p.D;
@@ -301,7 +304,22 @@ __device__ bool tail_piece(const CsmParams& p, int u, int piece, int32_t epoch, 
     T* const Vg = static_cast<T*>(p.V);
     uint8_t* const sK = stage;
     uint8_t* const sV = stage + kTailRows * RB;
-    {
+    if constexpr (PAGED) {
+        for (int i = tid; i < nrows * PR; i += blockDim.x) {
+            const int q = i / PR, k = i - q * PR;
+            const long long pr = map_row(p.rm, u, r0 + q);
+            if (pr < 0) {
+                if (k == 0) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                continue;
+            }
+            reinterpret_cast<uint4*>(sK)[i] = reinterpret_cast<const uint4*>(Kg + pr * D)[k];
+            reinterpret_cast<uint4*>(sV)[i] = reinterpret_cast<const uint4*>(Vg + pr * D)[k];
+        }
+        for (int q = tid; q < nrows; q += blockDim.x) {
+            const long long pr = map_row(p.rm, u, r0 + q);
+            sN[q] = pr < 0 ? 0 : p.N[pr];
+        }
+    } else {
         const uint4* srcK = reinterpret_cast<const uint4*>(Kg + (urow + r0) * D);
         const uint4* srcV = reinterpret_cast<const uint4*>(Vg + (urow + r0) * D);
         for (int i = tid; i < nrows * PR; i += blockDim.x) {
@@ -332,17 +350,35 @@ __device__ bool tail_piece(const CsmParams& p, int u, int piece, int32_t epoch, 
         }
     }
     if (!__syncthreads_and(okw)) return false;
-    uint4* dstK = reinterpret_cast<uint4*>(Kg + (urow + d0) * D);
-    uint4* dstV = reinterpret_cast<uint4*>(Vg + (urow + d0) * D);
-    for (int i = tid; i < nrows * PR; i += blockDim.x) {
-        dstK[i] = reinterpret_cast<const uint4*>(sK)[i];
-        dstV[i] = reinterpret_cast<const uint4*>(sV)[i];
+    if constexpr (PAGED) {
+        for (int i = tid; i < nrows * PR; i += blockDim.x) {
+            const int q = i / PR, k = i - q * PR;
+            const long long pr = map_row(p.rm, u, d0 + q);
+            if (pr < 0) {
+                if (k == 0) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                continue;
+            }
+            reinterpret_cast<uint4*>(Kg + pr * D)[k] = reinterpret_cast<const uint4*>(sK)[i];
+            reinterpret_cast<uint4*>(Vg + pr * D)[k] = reinterpret_cast<const uint4*>(sV)[i];
+        }
+        for (int q = tid; q < nrows; q += blockDim.x) {
+            const long long pr = map_row(p.rm, u, d0 + q);
+            if (pr >= 0) p.N[pr] = sN[q];
+        }
+    } else {
+        uint4* dstK = reinterpret_cast<uint4*>(Kg + (urow + d0) * D);
+        uint4* dstV = reinterpret_cast<uint4*>(Vg + (urow + d0) * D);
+        for (int i = tid; i < nrows * PR; i += blockDim.x) {
+            dstK[i] = reinterpret_cast<const uint4*>(sK)[i];
+            dstV[i] = reinterpret_cast<const uint4*>(sV)[i];
+        }
+        for (int q = tid; q < nrows; q += blockDim.x) p.N[urow + d0 + q] = sN[q];
     }
-    for (int q = tid; q < nrows; q += blockDim.x) p.N[urow + d0 + q] = sN[q];
     return true;
 }
 
-// Tensor-core launcher: three CTAs per SM with one slot each (csm_tc3.cu).
-int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st);
+// Tensor-core launcher: three CTAs per SM with one slot each (csm_tc3.cu);
+// paged: the block-table variant.
+int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, bool paged, cudaStream_t st);
 
 }  // namespace csmkv

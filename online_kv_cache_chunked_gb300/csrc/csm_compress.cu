@@ -235,12 +235,16 @@ extern "C" size_t csm_workspace_bytes(const csmkv_cache* cache, int32_t n1, int3
     return csm_layout(cache, n1, n2, c, &a, &b, &d, &e, &f, &L);
 }
 
-extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
-                               int32_t n1, int32_t n2, int32_t c, double r, const uint8_t* head_mask,
-                               const uint8_t* seq_mask, int32_t* match_out, const csm_options* opts,
-                               void* workspace, size_t ws_bytes, void* stream) {
+static int compress_impl(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+                         const csmkv_pages* pages, int32_t n1, int32_t n2, int32_t c, double r,
+                         const uint8_t* head_mask, const uint8_t* seq_mask, int32_t* match_out,
+                         const csm_options* opts, void* workspace, size_t ws_bytes, void* stream) {
     int rc = check_cache(cache);
     if (rc != CSMKV_OK) return rc;
+    if (pages) {
+        rc = check_pages(cache, pages);
+        if (rc != CSMKV_OK) return rc;
+    }
     if (!K || !V || !N || !len) return CSMKV_ERR_ARG;
     if (!aligned16(K) || !aligned16(V) || !aligned16(N) || (reinterpret_cast<uintptr_t>(len) & 3u))
         return CSMKV_ERR_ALIGN;
@@ -252,8 +256,10 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     int32_t L;
     const size_t need = csm_layout(cache, n1, n2, c, &o_snap, &o_ch, &o_tp, &o_fkn, &o_fv, &L);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CSMKV_ERR_WORKSPACE;
-    const int want = opts ? opts->kernel : CSM_KERNEL_AUTO;
+    const int want = pages ? CSM_KERNEL_TC_SPLIT : (opts ? opts->kernel : CSM_KERNEL_AUTO);
     if (want != CSM_KERNEL_AUTO && want != CSM_KERNEL_SIMT && want != CSM_KERNEL_TC_SPLIT) return CSMKV_ERR_ARG;
+    const bool tc_shape = cache->dtype == CSMKV_BF16 && c == 256 && (cache->head_dim == 64 || cache->head_dim == 128);
+    if (pages && !tc_shape) return CSMKV_ERR_UNSUPPORTED;  // the block-table variant is the tensor-core kernel
     const int32_t maxch = csm_max_chunks(cache, n1, n2, c);
     if (m == 0 || maxch == 0) return CSMKV_OK;  // nothing can merge
 
@@ -283,6 +289,7 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
     P.m = m;
     P.maxch = maxch;
     P.L = L;
+    P.rm = row_map(cache, pages);
     P.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : 2000000000LL;
     P.withhold = opts ? opts->withhold_signals : 0;
 
@@ -292,8 +299,9 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
 
     const int D = cache->head_dim;
     const bool tc = cache->dtype == CSMKV_BF16 && c == 256 && (D == 64 || D == 128) && want != CSM_KERNEL_SIMT;
-    const uint64_t rows = (uint64_t)cache->batch * cache->h_kv * cache->cap;
-    if (tc) return launch_csm_tc3(P, D, K, V, N, rows, st);
+    const uint64_t rows =
+        pages ? (uint64_t)pages->num_pages * pages->page_rows : (uint64_t)cache->batch * cache->h_kv * cache->cap;
+    if (tc) return launch_csm_tc3(P, D, K, V, N, rows, pages != nullptr, st);
     const int RB = D * (int)dtype_bytes(cache->dtype);
     const int smem = csm_stage_bytes_simt(c, RB) + (int)sizeof(CsmTables) + 257 * 4 + 1024;
     if (smem > 227 * 1024) return CSMKV_ERR_UNSUPPORTED;
@@ -305,6 +313,23 @@ extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const
         csm_simt_kernel<float><<<sm_count(), kCsmThreads, smem, st>>>(P);
     }
     return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
+}
+
+extern "C" int csm_compress_ex(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+                               int32_t n1, int32_t n2, int32_t c, double r, const uint8_t* head_mask,
+                               const uint8_t* seq_mask, int32_t* match_out, const csm_options* opts,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    return compress_impl(K, V, N, len, cache, nullptr, n1, n2, c, r, head_mask, seq_mask, match_out, opts, workspace,
+                         ws_bytes, stream);
+}
+
+extern "C" int csm_compress_paged(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache,
+                                  const csmkv_pages* pages, int32_t n1, int32_t n2, int32_t c, double r,
+                                  const uint8_t* head_mask, const uint8_t* seq_mask, int32_t* match_out,
+                                  const csm_options* opts, void* workspace, size_t ws_bytes, void* stream) {
+    if (!pages) return CSMKV_ERR_ARG;
+    return compress_impl(K, V, N, len, cache, pages, n1, n2, c, r, head_mask, seq_mask, match_out, opts, workspace,
+                         ws_bytes, stream);
 }
 
 extern "C" int csm_compress(void* K, void* V, int32_t* N, int32_t* len, const csmkv_cache* cache, int32_t n1,

@@ -20,6 +20,10 @@
 // In-place safety: every item publishes an epoch-tagged "loaded" flag per array
 // once its TMA lands; an item writes an array only after the items whose source
 // rows it overwrites have published (see csm_compress.cu).
+// PAGED (block-table layout): a chunk's rows are gathered row by row through the
+// unit's block table with 16-byte cp.async into the same swizzled operand layout,
+// and every output row is stored through the table; the flags and the order of
+// the in-place writes are those of the dense layout, in logical rows.
 #include "csm_common.cuh"
 
 namespace csmkv {
@@ -44,7 +48,7 @@ struct Tc3 {
     static constexpr int kSmem = kSlotBytes + kNStride + (int)sizeof(CsmTables) + (int)sizeof(Tc3State) + 1024;
 };
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kTc3Threads, 3)
     csm_tc3_kernel(const __grid_constant__ CsmParams p, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmN,
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
     // m < H: the c - m output rows (copies, or merged B rows) written straight to
     // global memory; as merge_inplace, two 16-byte pieces per thread in a
     // bank-distinct order, so the per-row lookups are paid once per 32 bytes.
-    auto emit_rows2 = [&](T* dst_rows, const int32_t* sN) {
+    auto emit_rows2 = [&](auto rowptr, const int32_t* sN) {  // rowptr(output row) -> T*, or nullptr: skip
         constexpr int TPR = 4 * R::kBoxes;
         const int sub = tid % TPR;
         const int box = sub >> 2;
@@ -217,7 +221,9 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
                     v1 = Elem<T>::pack(acc1);
                 }
             }
-            uint4* const drow = reinterpret_cast<uint4*>(dst_rows + (size_t)pr * D) + box * 8;
+            T* const rp = rowptr(pr);
+            if (!rp) continue;
+            uint4* const drow = reinterpret_cast<uint4*>(rp) + box * 8;
             drow[c0] = v0;
             drow[c1] = v1;
         }
@@ -228,6 +234,40 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
         bulk_commit();
         stores_pend = true;
     };
+    // PAGED: chunk row tid (c == 256 rows, one per thread) of unit u from logical row
+    // base, through the block table, into the swizzled A / B operand layout; its
+    // degree into nbuf[tid]. Completed by cp_async_wait_all.
+    auto gather_slot = [&](const T* arr, int u, int base, bool with_degrees) {  // all threads
+        const int q = tid, op = q & 1, r2 = q >> 1;
+        const long long pr = map_row(p.rm, u, base + q);
+        if (pr < 0) {
+            record_status(status, CSMKV_ERR_ARG);
+            if (with_degrees) nbuf[q] = 0;
+            return;
+        }
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(arr + pr * D);
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) {
+            const int bx = k >> 3, c16 = k & 7;
+            cp_async16(slot + (op * R::kBoxes + bx) * 16384 + r2 * 128 + ((c16 ^ (r2 & 7)) << 4), src + k * 16);
+        }
+        if (with_degrees) cp_async4(nbuf + q, p.N + pr);
+    };
+    // PAGED: the 128 B rows of the slot (the output when every A row merges) stored
+    // through the block table to logical rows drow .. drow + 127.
+    auto store_b_rows_paged = [&](T* arr, int u, int drow) {  // all threads
+        constexpr int PPR = D / 8;
+        for (int i = tid; i < 128 * PPR; i += kTc3Threads) {
+            const int b = i / PPR, k = i - (i / PPR) * PPR, bx = k >> 3, c16 = k & 7;
+            const long long pr = map_row(p.rm, u, drow + b);
+            if (pr < 0) {
+                record_status(status, CSMKV_ERR_ARG);
+                continue;
+            }
+            reinterpret_cast<uint4*>(arr + pr * D)[k] =
+                *reinterpret_cast<const uint4*>(slot + (R::kBoxes + bx) * 16384 + b * 128 + ((c16 ^ (b & 7)) << 4));
+        }
+    };
 
     for (;;) {
         if (tid == 0) {
@@ -237,7 +277,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
                 bulk_wait_read_all();
                 stores_pend = false;
             }
-            if (t != INT_MAX && t / BH < levels_ch) {
+            if (!PAGED && t != INT_MAX && t / BH < levels_ch) {
                 const int j = t / BH, u = t - j * BH;
                 load_slot(&tmK, (long long)u * p.cap + p.n1 + (long long)j * c, true);
             }
@@ -247,6 +287,9 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
         if (t == INT_MAX) break;
         const int lev = t / BH, u = t - lev * BH;
         bool ok = true;
+        if constexpr (PAGED) {
+            if (lev < levels_ch) gather_slot(Kg, u, p.n1 + lev * c, true);
+        }
 
         if (lev < levels_ch) {
             // ================================================================ chunk item
@@ -254,7 +297,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             const size_t urow = (size_t)u * p.cap;
             const int dst_row = p.n1 + j * (c - m);
             const long long g0 = (long long)urow + p.n1 + (long long)j * c;
-            const int32_t* const sN = nbuf + (int)(g0 & 3);
+            const int32_t* const sN = PAGED ? nbuf : nbuf + (int)(g0 & 3);
             int32_t* const fkn = p.flag_kn + (size_t)u * p.L;
             int32_t* const fv = p.flag_v + (size_t)u * p.L;
             int lo, hi;
@@ -273,8 +316,13 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             }
 
             // (1) K and degrees on chip
-            ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
-            phase ^= 1u;
+            if constexpr (PAGED) {
+                cp_async_wait_all();
+                fence_proxy_async_smem();  // the gathered operands before the MMA reads them
+            } else {
+                ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
+                phase ^= 1u;
+            }
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
             if (tid == 0) load_pend = false;
             if (publisher) publish(fkn + j, epoch, p.withhold);
@@ -371,26 +419,50 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             }
             if (all) {
                 merge_inplace(sN);
-                fence_proxy_async_smem();
-                __syncthreads();
-                if (tid == 0) store_b_rows(&tmKs, (long long)urow + dst_row);
+                if constexpr (PAGED) {
+                    __syncthreads();
+                    store_b_rows_paged(Kg, u, dst_row);
+                } else {
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                    if (tid == 0) store_b_rows(&tmKs, (long long)urow + dst_row);
+                }
+            } else if constexpr (PAGED) {
+                emit_rows2([&](int pr) -> T* {
+                    const long long r = map_row(p.rm, u, dst_row + pr);
+                    if (r < 0) record_status(status, CSMKV_ERR_ARG);
+                    return r < 0 ? nullptr : Kg + r * D;
+                }, sN);
             } else {
-                emit_rows2(Kg + (urow + dst_row) * D, sN);
+                emit_rows2([&](int pr) -> T* { return Kg + (urow + dst_row + pr) * D; }, sN);
             }
-            emit_degrees(p.N + urow + dst_row, c - m, m, sm, sN);
+            if constexpr (PAGED) {
+                for (int pr = tid; pr < c - m; pr += kTc3Threads) {
+                    const int q = all ? 2 * pr + 1 : sm.src[pr];
+                    const long long r = map_row(p.rm, u, dst_row + pr);
+                    if (r >= 0) p.N[r] = (q & 1) ? sm.nsum[q >> 1] : sN[q];
+                }
+            } else {
+                emit_degrees(p.N + urow + dst_row, c - m, m, sm, sN);
+            }
 
             // (6) V through the same slot once the K output has left it
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0) {
-                if (stores_pend) {
-                    bulk_wait_read_all();
-                    stores_pend = false;
+            if constexpr (PAGED) {
+                gather_slot(Vg, u, p.n1 + j * c, false);
+                cp_async_wait_all();
+            } else {
+                if (tid == 0) {
+                    if (stores_pend) {
+                        bulk_wait_read_all();
+                        stores_pend = false;
+                    }
+                    load_slot(&tmV, g0, false);
                 }
-                load_slot(&tmV, g0, false);
+                ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
+                phase ^= 1u;
             }
-            ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
-            phase ^= 1u;
             if (!__syncthreads_and(ok)) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
             if (tid == 0) load_pend = false;
             if (publisher) publish(fv + j, epoch, p.withhold);
@@ -400,15 +472,25 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             }
             if (all) {
                 merge_inplace(sN);
-                fence_proxy_async_smem();
-                __syncthreads();
-                if (tid == 0) store_b_rows(&tmVs, (long long)urow + dst_row);
+                if constexpr (PAGED) {
+                    __syncthreads();
+                    store_b_rows_paged(Vg, u, dst_row);
+                } else {
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                    if (tid == 0) store_b_rows(&tmVs, (long long)urow + dst_row);
+                }
+            } else if constexpr (PAGED) {
+                emit_rows2([&](int pr) -> T* {
+                    const long long r = map_row(p.rm, u, dst_row + pr);
+                    return r < 0 ? nullptr : Vg + r * D;
+                }, sN);
             } else {
-                emit_rows2(Vg + (urow + dst_row) * D, sN);
+                emit_rows2([&](int pr) -> T* { return Vg + (urow + dst_row + pr) * D; }, sN);
             }
         } else {
             // ================================================================ tail piece
-            ok = tail_piece<T>(p, u, lev - levels_ch, epoch, slot, nbuf);
+            ok = tail_piece<T, PAGED>(p, u, lev - levels_ch, epoch, slot, nbuf);
             if (!ok) { record_status(status, CSMKV_ERR_TIMEOUT); break; }
         }
         fence_proxy_async_smem();  // the next TMA overwrites the slot
@@ -427,7 +509,7 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, cudaStream_t st) {
+int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint64_t rows, bool paged, cudaStream_t st) {
     CUtensorMap tmK{}, tmV{}, tmN{}, tmKs{}, tmVs{};
     const uint64_t dims[3] = {(uint64_t)D, 2, rows / 2};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
@@ -453,7 +535,9 @@ int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint
             return (int)CSMKV_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? (int)CSMKV_OK : (int)CSMKV_ERR_CUDA;
     };
-    return D == 128 ? run(csm_tc3_kernel<128>, Tc3<128>::kSmem) : run(csm_tc3_kernel<64>, Tc3<64>::kSmem);
+    if (paged)
+        return D == 128 ? run(csm_tc3_kernel<128, true>, Tc3<128>::kSmem) : run(csm_tc3_kernel<64, true>, Tc3<64>::kSmem);
+    return D == 128 ? run(csm_tc3_kernel<128, false>, Tc3<128>::kSmem) : run(csm_tc3_kernel<64, false>, Tc3<64>::kSmem);
 }
 
 }  // namespace csmkv

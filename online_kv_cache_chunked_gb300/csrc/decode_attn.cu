@@ -110,6 +110,8 @@ struct DecParams {
     float* pm;            // [splits][G] running max (base-2 domain)
     float* pl;            // [splits][G] running sum
     float* pacc;          // [splits][G][D] unnormalised output
+    RowMap rm;            // logical row -> pool row (dense, or through a block table)
+    int32_t pool_rows;    // rows of the K / V / N tensors the TMA maps cover
     int32_t BH, Hkv, Hq, G, cap, D, nCTA, max_splits;
     float scale_log2;     // scale * log2(e)
     float scale;          // natural-log scale (fp32 path)
@@ -571,10 +573,31 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             const int ntok = cur.ntok;
             const int ntiles = (ntok + kTile - 1) / kTile;
             const long long row_base = (long long)cur.u * p.cap;
+            // paged layout: the ids of the pages from pg_base on, one per lane (the
+            // window moves when a tile runs past it); every lane calls pool_row
+            int pg_base = 0, pg_id = -1;
+            auto load_pages = [&](int first_page) {
+                pg_base = first_page;
+                const int pi = first_page + lane;
+                pg_id = pi < p.rm.maxp ? __ldg(p.rm.table + (size_t)cur.u * p.rm.maxp + pi) : -1;
+            };
+            if (p.rm.table) load_pages(tok0 / p.rm.P);
+            auto pool_row = [&](int t) -> long long {  // -1: a block-table entry outside the pool
+                if (!p.rm.table) return row_base + t;
+                const int pi = t / p.rm.P;
+                if (pi - pg_base >= 32) load_pages(pi);
+                const int pg = __shfl_sync(0xffffffffu, pg_id, pi - pg_base);
+                return (pg < 0 || pg >= p.rm.npages) ? -1 : (long long)pg * p.rm.P + t % p.rm.P;
+            };
             int arow = -1;  // fused append: the unit's new row, held by its last split
+            long long arow_p = -1;
             if (p.k_new && cur.k == cur.n - 1) {
                 const int old = p.len[cur.u];
                 if (old >= 0 && old < p.cap) arow = old;
+                if (arow >= 0) {
+                    arow_p = pool_row(arow);
+                    if (arow_p < 0 && lane == 0) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                }
             }
             for (int i = 0; i < ntiles; ++i) {
                 const int s = issued % kStages;
@@ -597,7 +620,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                 }
                 const int tok = tok0 + i * kTile;
                 const int nv = min(kTile, ntok - i * kTile);
-                if (arow >= tok && arow < tok + nv) {
+                const long long prow = pool_row(tok);
+                if (arow >= tok && arow < tok + nv && arow_p >= 0) {
                     // the new token's K, V row and degree, written before the TMA reads the
                     // tile (one 16-byte piece per lane; the fence orders each lane's writes
                     // before the async-proxy reads that follow the warp sync)
@@ -606,9 +630,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                         const bool isv = lane >= PPR;
                         const int kk = isv ? lane - PPR : lane;
                         const uint4* src = static_cast<const uint4*>(isv ? p.v_new : p.k_new) + (size_t)cur.u * PPR + kk;
-                        uint4* dst = static_cast<uint4*>(isv ? p.V : p.K) + (size_t)(row_base + arow) * PPR + kk;
+                        uint4* dst = static_cast<uint4*>(isv ? p.V : p.K) + (size_t)arow_p * PPR + kk;
                         *dst = *src;
-                        if (lane == 0) p.N[row_base + arow] = 1;
+                        if (lane == 0) p.N[arow_p] = 1;
                         fence_proxy_async_global();
                     }
                     __syncwarp();
@@ -622,7 +646,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                     mt.tok = tok;
                     mt.nv = nv;
                     mt.flags = (i == 0 ? kFirst : 0u) | (i == ntiles - 1 ? kLast : 0u);
-                    const int row = (int)(row_base + tok);
+                    // a tile whose page entry is outside the pool reads the fill value (zeros)
+                    if (prow < 0) record_status(&p.hdr->status, CSMKV_ERR_ARG);
+                    const int row = prow < 0 ? p.pool_rows : (int)prow;
                     uint8_t* st = sbase + s * Geo::kStageBytes;
                     // the first tile of a split also brings the group's query rows
                     const uint32_t qbytes = i == 0 ? (uint32_t)(p.G * D * 2) : 0u;
@@ -985,10 +1011,15 @@ extern "C" size_t decode_attn_workspace_bytes(const csmkv_cache* cache, int32_t 
 // Attention over the cache, optionally with the step's new token appended first
 // (k_new != NULL: bf16 fuses the append into the attention kernel).
 static int decode_attn_impl(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
-                            const void* k_new, const void* v_new, const csmkv_cache* cache, int32_t h_q, float scale,
-                            void* out, void* workspace, size_t ws_bytes, void* stream) {
+                            const void* k_new, const void* v_new, const csmkv_cache* cache, const csmkv_pages* pages,
+                            int32_t h_q, float scale, void* out, void* workspace, size_t ws_bytes, void* stream) {
     int rc = decode_attn_check_args(q, K, V, N, len, k_new, v_new, cache, h_q, scale, out);
     if (rc != CSMKV_OK) return rc;
+    if (pages) {
+        rc = check_pages(cache, pages);
+        if (rc != CSMKV_OK) return rc;
+        if (cache->dtype != CSMKV_BF16) return CSMKV_ERR_UNSUPPORTED;
+    }
     const int G = h_q / cache->h_kv;
     const int D = cache->head_dim;
     const bool bf16 = cache->dtype == CSMKV_BF16;
@@ -1025,6 +1056,7 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
     P.D = D;
     P.nCTA = nCTA;
     P.max_splits = dec_max_splits(nCTA, P.BH);
+    P.rm = row_map(cache, pages);
     P.scale = scale;
     P.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1041,7 +1073,9 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
         return cudaGetLastError() == cudaSuccess ? CSMKV_OK : CSMKV_ERR_CUDA;
     }
 
-    const uint64_t rows = (uint64_t)cache->batch * cache->h_kv * cache->cap;
+    const uint64_t rows =
+        pages ? (uint64_t)pages->num_pages * pages->page_rows : (uint64_t)cache->batch * cache->h_kv * cache->cap;
+    P.pool_rows = (int32_t)rows;
     CUtensorMap tk{}, tv{}, tn{};
     {
         const uint64_t dims[2] = {(uint64_t)D, rows};
@@ -1071,12 +1105,32 @@ static int decode_attn_impl(const void* q, const void* K, const void* V, const i
 extern "C" int decode_attn_logn(const void* q, const void* K, const void* V, const int32_t* N, const int32_t* len,
                                 const csmkv_cache* cache, int32_t h_q, float scale, void* out, void* workspace,
                                 size_t ws_bytes, void* stream) {
-    return decode_attn_impl(q, K, V, N, len, nullptr, nullptr, cache, h_q, scale, out, workspace, ws_bytes, stream);
+    return decode_attn_impl(q, K, V, N, len, nullptr, nullptr, cache, nullptr, h_q, scale, out, workspace, ws_bytes,
+                            stream);
+}
+
+extern "C" int decode_attn_logn_paged(const void* q, const void* K, const void* V, const int32_t* N,
+                                      const int32_t* len, const csmkv_cache* cache, const csmkv_pages* pages,
+                                      int32_t h_q, float scale, void* out, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+    if (!pages) return CSMKV_ERR_ARG;
+    return decode_attn_impl(q, K, V, N, len, nullptr, nullptr, cache, pages, h_q, scale, out, workspace, ws_bytes,
+                            stream);
 }
 
 extern "C" int decode_step_logn(const void* q, const void* k_new, const void* v_new, void* K, void* V, int32_t* N,
                                 int32_t* len, const csmkv_cache* cache, int32_t h_q, float scale, void* out,
                                 void* workspace, size_t ws_bytes, void* stream) {
     if (!k_new || !v_new) return CSMKV_ERR_ARG;
-    return decode_attn_impl(q, K, V, N, len, k_new, v_new, cache, h_q, scale, out, workspace, ws_bytes, stream);
+    return decode_attn_impl(q, K, V, N, len, k_new, v_new, cache, nullptr, h_q, scale, out, workspace, ws_bytes,
+                            stream);
+}
+
+extern "C" int decode_step_logn_paged(const void* q, const void* k_new, const void* v_new, void* K, void* V,
+                                      int32_t* N, int32_t* len, const csmkv_cache* cache, const csmkv_pages* pages,
+                                      int32_t h_q, float scale, void* out, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+    if (!k_new || !v_new || !pages) return CSMKV_ERR_ARG;
+    return decode_attn_impl(q, K, V, N, len, k_new, v_new, cache, pages, h_q, scale, out, workspace, ws_bytes,
+                            stream);
 }

@@ -45,6 +45,11 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
     if (rc != CSMKV_OK) return rc;
     if ((L->l2_flush == nullptr) != (L->l2_flush_bytes == 0)) return CSMKV_ERR_ARG;
     if (L->l2_flush && (!csmkv::aligned16(L->l2_flush) || L->l2_flush_bytes % 16 != 0)) return CSMKV_ERR_ALIGN;
+    const csmkv_pages* const pg = L->pages;  // block-table layout: the paged entry points, fused steps
+    if (pg) {
+        if (!L->fused_append) return CSMKV_ERR_ARG;
+        if ((rc = csmkv::check_pages(&L->cache, pg)) != CSMKV_OK) return rc;
+    }
 
     const csmkv_cache& C = L->cache;
     const size_t eb = cache_elem_bytes(C);
@@ -74,11 +79,15 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
         if ((rc = record(L->attn_events, 2 * attn_k, st)) != CSMKV_OK) return rc;
         const uint8_t* const qs = static_cast<const uint8_t*>(L->q) + s * q_step;
         uint8_t* const os = static_cast<uint8_t*>(L->out) + s * q_step;
-        rc = L->fused_append
-                 ? decode_step_logn(qs, kn, vn, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
-                                    L->ws_attn_bytes, stream)
-                 : decode_attn_logn(qs, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
-                                    L->ws_attn_bytes, stream);
+        if (pg)
+            rc = decode_step_logn_paged(qs, kn, vn, L->K, L->V, L->N, L->len, &C, pg, L->h_q, L->scale, os,
+                                        L->ws_attn, L->ws_attn_bytes, stream);
+        else
+            rc = L->fused_append
+                     ? decode_step_logn(qs, kn, vn, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
+                                        L->ws_attn_bytes, stream)
+                     : decode_attn_logn(qs, L->K, L->V, L->N, L->len, &C, L->h_q, L->scale, os, L->ws_attn,
+                                        L->ws_attn_bytes, stream);
         if (rc != CSMKV_OK) return rc;
         if ((rc = record(L->attn_events, 2 * attn_k + 1, st)) != CSMKV_OK) return rc;
         ++attn_k;
@@ -86,8 +95,10 @@ extern "C" int csm_decode_run(const csm_decode_loop* L, int32_t first_step, int3
             const csm_round_plan& R = L->rounds[ri];
             if ((rc = record(L->csm_events, 2 * csm_k, st)) != CSMKV_OK) return rc;
             opts.seq_max_chunks = R.seq_max_chunks;
-            rc = csm_compress_ex(L->K, L->V, L->N, L->len, &C, L->n1, L->n2, L->c, R.r, L->head_mask, R.seq_mask,
-                                 nullptr, &opts, L->ws_csm, L->ws_csm_bytes, stream);
+            rc = pg ? csm_compress_paged(L->K, L->V, L->N, L->len, &C, pg, L->n1, L->n2, L->c, R.r, L->head_mask,
+                                         R.seq_mask, nullptr, &opts, L->ws_csm, L->ws_csm_bytes, stream)
+                    : csm_compress_ex(L->K, L->V, L->N, L->len, &C, L->n1, L->n2, L->c, R.r, L->head_mask, R.seq_mask,
+                                      nullptr, &opts, L->ws_csm, L->ws_csm_bytes, stream);
             if (rc != CSMKV_OK) return rc;
             if ((rc = record(L->csm_events, 2 * csm_k + 1, st)) != CSMKV_OK) return rc;
             ++csm_k;

@@ -66,6 +66,36 @@ inline int check_cache(const csmkv_cache* c) {
     return CSMKV_OK;
 }
 
+// Validates a paged layout against the logical cache descriptor.
+inline int check_pages(const csmkv_cache* c, const csmkv_pages* pg) {
+    if (!pg || !pg->table) return CSMKV_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(pg->table) & 3u) return CSMKV_ERR_ALIGN;
+    if (pg->page_rows < 64 || (pg->page_rows % 64) != 0 || pg->max_pages < 1 || pg->num_pages < 1)
+        return CSMKV_ERR_ARG;
+    if ((long long)pg->max_pages * pg->page_rows != c->cap) return CSMKV_ERR_ARG;
+    if ((long long)pg->num_pages * pg->page_rows > 0x7FFFFFFFLL) return CSMKV_ERR_ARG;  // pool rows are int32
+    return CSMKV_OK;
+}
+
+// Logical row -> pool row of a cache: unit-major dense rows (table == nullptr),
+// or a paged layout's block table. Plain data, passed to kernels by value.
+struct RowMap {
+    const int32_t* table;
+    int32_t P, maxp, npages, cap;
+};
+
+inline RowMap row_map(const csmkv_cache* c, const csmkv_pages* pg) {
+    RowMap m{};
+    m.cap = c->cap;
+    if (pg) {
+        m.table = pg->table;
+        m.P = pg->page_rows;
+        m.maxp = pg->max_pages;
+        m.npages = pg->num_pages;
+    }
+    return m;
+}
+
 int sm_count();                 // SMs of the current device (cached per device)
 // Raises a kernel's dynamic shared-memory limit on the current device (and, if
 // asked, prefers the largest shared-memory carveout). The setting is remembered

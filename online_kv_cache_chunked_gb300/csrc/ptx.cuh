@@ -53,6 +53,26 @@ __device__ __forceinline__ bool wait_flag(const int32_t* flag, int32_t want, uin
     }
 }
 
+// Pool row of logical row r of unit u (see RowMap in host_util.h), or -1 when the
+// block-table entry is outside the pool (the caller skips the access).
+template <typename Map>
+__device__ __forceinline__ long long map_row(const Map& m, int u, int r) {
+    if (!m.table) return (long long)u * m.cap + r;
+    const int pg = __ldg(m.table + (size_t)u * m.maxp + r / m.P);
+    if (pg < 0 || pg >= m.npages) return -1;
+    return (long long)pg * m.P + r % m.P;
+}
+
+// Non-bulk asynchronous copies global -> shared (16 bytes, L2 only; 4 bytes).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+// Waits for every cp.async this thread issued.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -100,17 +100,21 @@ class Pipeline:
     data: dict from synth.make_device / synth.cache_from_numpy (K, V, N, len,
     k_dec, v_dec, q, head_mask). The cache tensors are updated in place; the
     attention output of decode step i lands in self.out[i].
+    paged: optional binding.PagedKV holding the same cache in a block-table layout;
+    every call then goes to the paged entry points (fused decode steps) and the
+    dense K, V, N of `data` are not used.
     """
 
-    def __init__(self, w, data, stream=None, csm_kernel=B.CSM_KERNEL_AUTO):
+    def __init__(self, w, data, stream=None, csm_kernel=B.CSM_KERNEL_AUTO, paged=None):
         self.w = w
         self.d = data
         self.stream = stream
         self.csm_kernel = int(csm_kernel)
+        self.paged = paged
         self.rounds = plan(w)
-        K = data["K"]
+        K = paged.K if paged is not None else data["K"]
         dev = K.device
-        cache = B.cache_desc(K)
+        cache = paged.cache() if paged is not None else B.cache_desc(K)
         self.ws_csm = B.new_workspace(B.csm_workspace_bytes(cache, w.n1, w.n2, w.c), dev)
         self.ws_app = B.new_workspace(B.csm_append_workspace_bytes(), dev)
         self.ws_att = B.new_workspace(B.decode_attn_workspace_bytes(cache, w.h_q), dev)
@@ -149,7 +153,10 @@ class Pipeline:
             rd = self.rounds[k]
             if hook:
                 hook("csm", rd, True)
-            if self.csm_kernel == B.CSM_KERNEL_AUTO and self.limits[k] is None:
+            if self.paged is not None:
+                B.csm_compress_paged(self.paged, d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask, self.masks[k],
+                                     seq_max_chunks=self.limits[k], workspace=self.ws_csm, stream=self.stream)
+            elif self.csm_kernel == B.CSM_KERNEL_AUTO and self.limits[k] is None:
                 B.csm_compress(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rd.r, self.head_mask,
                                self.masks[k], self.ws_csm, self.stream)
             else:
@@ -162,6 +169,8 @@ class Pipeline:
     def decode_step(self, i, hook=None):
         """Decode step i (1-based): append, attend, then the trigger's rounds."""
         d = self.d
+        if self.paged is not None:
+            raise ValueError("a paged pipeline issues its decode steps natively (decode_native)")
         B.csm_append(d["K"], d["V"], d["N"], d["len"], d["k_dec"][i - 1], d["v_dec"][i - 1], None, self.ws_app,
                      self.stream)
         if hook:
@@ -187,11 +196,13 @@ class Pipeline:
         call, with the rounds the plan fires at those steps (fused: each step's append
         and attention as one kernel)."""
         d, w = self.d, self.w
-        B.csm_decode_run(d["K"], d["V"], d["N"], d["len"], d["q"], d["k_dec"], d["v_dec"], self.out, w.n1, w.n2,
+        kv = self.paged
+        K, V, N = (kv.K, kv.V, kv.N) if kv is not None else (d["K"], d["V"], d["N"])
+        B.csm_decode_run(K, V, N, d["len"], d["q"], d["k_dec"], d["v_dec"], self.out, w.n1, w.n2,
                          w.c, rounds=self.decode_plan(), head_mask=self.head_mask, ws_csm=self.ws_csm,
                          ws_append=self.ws_app, ws_attn=self.ws_att, first_step=first_step, steps=steps,
                          csm_kernel=self.csm_kernel, attn_events=attn_events, csm_events=csm_events,
-                         l2_flush=l2_flush, stream=self.stream, fused_append=fused)
+                         l2_flush=l2_flush, stream=self.stream, fused_append=fused or kv is not None, paged=kv)
 
     def run_native(self, steps=None, hook=None, attn_events=None, csm_events=None, l2_flush=None, fused=True):
         """Prefill round(s), then the whole decode loop issued by the library in one call

@@ -38,7 +38,8 @@ def test_every_declared_symbol_is_exported(lib):
         "csm_append", "decode_attn_workspace_bytes", "decode_attn_logn", "decode_attn_logn_noalloc", "decode_step_logn",
         "csm_decode_run", "csm_budget", "csm_chunks_to_budget", "csm_should_trigger",
         "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
-        "csmkv_clear_status", "csmkv_status_str"]), names
+        "csmkv_clear_status", "csmkv_status_str", "csm_append_paged", "csm_compress_paged",
+        "decode_attn_logn_paged", "decode_step_logn_paged"]), names
     raw = ctypes.CDLL(_build.OUT)
     for n in names:
         assert hasattr(raw, n), f"{n} declared in csmkv.h but not exported"
@@ -175,3 +176,54 @@ def test_decode_run_rejects_bad_arguments_without_a_gpu(lib):
     loop.cache = B.Cache(1, 2, 128, 1024, 0)
     loop.l2_flush = x
     assert fn(ctypes.byref(loop), 1, 3, None) == 1  # a flush buffer without a size
+
+
+def test_paged_argument_errors_without_gpu(lib):
+    """The paged entry points check the block-table descriptor against the logical
+    cache before any launch."""
+    P = ctypes.c_void_p
+    c = _cache(cap=1024)  # logical: 4 pages of 256
+
+    def compress(pages, cache=c):
+        return lib.csm_compress_paged(P(4096), P(4096), P(4096), P(4096), ctypes.byref(cache),
+                                      ctypes.byref(pages) if pages is not None else None, 16, 64, 256, 0.5,
+                                      None, None, None, None, P(1 << 16), 1 << 20, None)
+
+    def attn(pages, cache=c):
+        return lib.decode_attn_logn_paged(P(4096), P(4096), P(4096), P(4096), P(4096), ctypes.byref(cache),
+                                          ctypes.byref(pages) if pages is not None else None, 8, 0.088, P(4096),
+                                          P(1 << 16), 1 << 24, None)
+    ok = B.Pages(4096, 256, 4, 64)
+    assert compress(None) == 1
+    assert compress(B.Pages(0, 256, 4, 64)) == 1         # no table
+    assert compress(B.Pages(4098, 256, 4, 64)) == 3      # misaligned table
+    assert compress(B.Pages(4096, 96, 4, 64)) == 1       # page_rows not a multiple of 64
+    assert compress(B.Pages(4096, 256, 3, 64)) == 1      # max_pages * page_rows != cap
+    assert compress(B.Pages(4096, 256, 4, 0)) == 1       # empty pool
+    assert compress(ok, _cache(cap=1024, dtype=1)) == 8  # fp32: the block-table variant is tensor-core only
+    assert attn(None) == 1
+    assert attn(ok, _cache(cap=1024, dtype=1)) == 8      # fp32 paged attention is not covered
+    assert attn(B.Pages(4096, 256, 4, 1 << 24)) == 1     # pool rows beyond int32
+    assert lib.csm_append_paged(P(4096), P(4096), P(4096), P(4096), ctypes.byref(c), None, P(4096), P(4096), None,
+                                P(1 << 16), 256, None) == 1
+
+
+def test_paged_layout_round_trip_on_cpu():
+    import torch
+
+    from online_kv_cache_chunked_gb300 import paged
+    g = torch.Generator().manual_seed(0)
+    K = torch.randn(2, 3, 512, 16, generator=g).to(torch.bfloat16)
+    V = torch.randn(2, 3, 512, 16, generator=g).to(torch.bfloat16)
+    N = torch.randint(1, 9, (2, 3, 512), generator=g, dtype=torch.int32)
+    kv = paged.to_paged(K, V, N, 128, spare_pages=5, seed=3)
+    assert kv.table.shape == (6, 4) and kv.K.shape == (6 * 4 + 5, 128, 16)
+    assert sorted(kv.table.view(-1).tolist()) == sorted(set(kv.table.view(-1).tolist()))  # no page twice
+    K2, V2, N2 = paged.to_dense(kv)
+    assert torch.equal(K2, K) and torch.equal(V2, V) and torch.equal(N2, N)
+    c = kv.cache()
+    assert (c.batch, c.h_kv, c.head_dim, c.cap) == (2, 3, 16, 512)
+    kv = paged.to_paged(K[:, :, :300], V[:, :, :300], N[:, :, :300], 128)  # cap rounded up to whole pages
+    assert kv.cap == 384
+    K2, _, N2 = paged.to_dense(kv)
+    assert torch.equal(K2[:, :, :300], K[:, :, :300]) and not N2[:, :, 300:].any()
