@@ -573,6 +573,46 @@ def e2e_measure_paged(w, d, kv, kv0, L0, p, rounds, args):
             "through the paged entry point, D2H of the pools (one stream, not pipelined)"}
 
 
+def host_link(up, down, reps=3):
+    """The host link's copy rates in this process (pinned buffers, copy engines): upload
+    alone, download alone, and both at once on two streams; GB/s, best of a few."""
+    import torch
+
+    nb = min(up.numel() * up.element_size(), down.numel() * down.element_size(), 1 << 30)
+    dv = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    u8 = up.view(-1).view(torch.uint8)[:nb]
+    d8 = down.view(-1).view(torch.uint8)[:nb]
+    half = nb // 2
+    s_up, s_dn = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, nbytes):
+        best = 0.0
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        return best
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s_up.wait_stream(cur)
+        s_dn.wait_stream(cur)
+        with torch.cuda.stream(s_up):
+            dv[:half].copy_(u8[:half], non_blocking=True)
+        with torch.cuda.stream(s_dn):
+            d8[half:2 * half].copy_(dv[half:2 * half], non_blocking=True)
+        cur.wait_stream(s_up)
+        cur.wait_stream(s_dn)
+
+    return {"h2d_gbs": timed(lambda: dv.copy_(u8, non_blocking=True), nb),
+            "d2h_gbs": timed(lambda: d8.copy_(dv, non_blocking=True), nb),
+            "both_gbs": timed(both, 2 * half), "bytes": int(nb)}
+
+
 def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     """CSM end to end from pinned host buffers: H2D of the prefill cache, the prefill
     round(s), D2H of the compacted rows (pipelined over groups of layers on separate
@@ -600,8 +640,9 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     # Pipelined by groups of cache rows (layers x sequences): group g's upload, its
     # prefill round(s) and its download run on three streams, so one group's
     # transfers overlap another's compression and the two copy directions overlap
-    # (a second upload stream was slower: the uploads share the host link).
-    G = max(1, min(8, w.batch))
+    # (a second upload stream was slower: the uploads share the host link). Smaller
+    # groups shorten the download of the last group, which nothing overlaps.
+    G = max(1, min(args.e2e_groups, w.batch))
     bounds = [(g * w.batch // G, (g + 1) * w.batch // G) for g in range(G)]
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     pre_k = [k for k, rd in enumerate(rounds) if rd.step == 0]
@@ -640,6 +681,8 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
             times.append(e0.elapsed_time(e1) / 1e3)
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
     d2h = sum(t.numel() * t.element_size() for t in (oK, oV, oN))
+    t_e2e = float(np.median(times))
+    link = host_link(hK, oK)
     # attention decode steps from host buffers: H2D of q, k, v; append; attend; D2H of o
     nsteps = min(50, w.steps)
     hq = d["q"][:nsteps].cpu().pin_memory()
@@ -663,9 +706,13 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     lens = d["len"].cpu().numpy()
     step_bytes = attn_bytes(w, lens - nsteps // 2)
     att_s = e0.elapsed_time(e1) / 1e3
-    return {"value": tokens / float(np.median(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+    # the host link's own rates bound this leg: the upload alone takes h2d / link h2d
+    bound = max(h2d / link["h2d_gbs"], (h2d + d2h) / link["both_gbs"]) / 1e9
+    return {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
-            "compress, D2H compacted rows, pipelined over groups of layers",
+            f"compress, D2H compacted rows, pipelined over {G} groups of cache rows",
+            "ms": t_e2e * 1e3, "h2d_gbs": h2d / t_e2e / 1e9, "host_link_gbs": (h2d + d2h) / t_e2e / 1e9,
+            "link": link, "link_bound_ms": bound * 1e3, "link_frac": bound / t_e2e,
             "decode_attn_gbs_at_prefill_round_length": step_bytes * nsteps / att_s / 1e9,
             "decode_step_h2d_bytes": int((dq.numel() * dq.element_size() + 2 * dk.numel() * dk.element_size()) // nsteps),
             "decode_step_d2h_bytes": int(ho[0].numel() * ho[0].element_size())}
@@ -692,6 +739,9 @@ def main():
                     help="run on a paged (block-table) copy of the cache: pages of --page-rows rows at scattered "
                          "pool pages")
     ap.add_argument("--page-rows", type=int, default=256)
+    ap.add_argument("--e2e-groups", type=int, default=32,
+                    help="the end-to-end leg pipelines uploads, compression and downloads over this many "
+                         "groups of cache rows")
     ap.add_argument("--shard", default="weak", choices=["weak", "strong"],
                     help="with N ranks: weak = N copies of the workload's shape, one per rank (per-GPU work "
                          "fixed); strong = the workload's own units split over the ranks")
