@@ -65,6 +65,8 @@ def _load():
         lib.oracle_append.restype = i32
         lib.oracle_decode_attn_logn.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32,
                                                 ctypes.c_double, P, i32]
+        lib.oracle_prefill_attn.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_double, P, i32,
+                                            P, i32]
         lib.oracle_max_threads.restype = i32
         _lib = lib
     return _lib
@@ -179,4 +181,24 @@ def decode_attn_logn(q, K, V, N, length, h_q: int, scale=None, nthreads=None):
     out = np.zeros((B, h_q, d))
     _load().oracle_decode_attn_logn(_ptr(q), _ptr(K), _ptr(V), _ptr(N), _ptr(L), B, Hkv, h_q,
                                     cap, d, float(scale), _ptr(out), _threads(nthreads))
+    return out
+
+
+def prefill_attn(q, K, V, n: int, h_q: int, scale=None, rows=None, nthreads=None):
+    """Causal prefill attention with every degree 1 ([Chelsea] §三 算法流程, Algorithm 1:
+    O = FlashAttn(Q, K, V) on the prompt). q: [B, Hq, n, d]; K, V: [B, Hkv, cap, d]
+    (rows 0..n-1 are the prompt). rows: query positions to evaluate (default all).
+    Returns o [B, Hq, len(rows), d] in fp64."""
+    K, V = _f64(K), _f64(V)
+    B, Hkv, cap, d = K.shape
+    q = _f64(q).reshape(B, h_q, n, d)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    r = None if rows is None else _i32(rows)
+    nrows = n if r is None else int(r.size)
+    if r is not None and (r.min(initial=0) < 0 or r.max(initial=0) >= n):
+        raise ValueError("query rows outside the prompt")
+    out = np.zeros((B, h_q, nrows, d))
+    _load().oracle_prefill_attn(_ptr(q), _ptr(K), _ptr(V), B, Hkv, h_q, n, cap, d, float(scale), _ptr(r), nrows,
+                                _ptr(out), _threads(nthreads))
     return out

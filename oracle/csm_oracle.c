@@ -31,6 +31,8 @@
  *   Degree-aware attention [Chelsea §三 核心公式]:
  *        O = softmax(q K^T / sqrt(d) + log N) V, computed literally with the
  *        log-degree bias and a max shift.
+ *   Prefill attention [Chelsea §三 算法流程, Algorithm 1]: the prompt's causal
+ *        softmax attention with every degree 1, before the first round.
  *
  * Arithmetic is fp64 throughout; degrees and lengths are int32.
  * Parallelism: OpenMP over independent (sequence, KV head) units or over an
@@ -429,6 +431,53 @@ void oracle_decode_attn_logn(const double* q, const double* K, const double* V,
             for (int32_t i = 0; i < d; ++i) o[i] += w * Vu[(size_t)t * d + i];
         }
         for (int32_t i = 0; i < d; ++i) o[i] /= den;
+        free(logit);
+    }
+}
+
+/*
+ * Prefill attention [Chelsea §三 算法流程, Algorithm 1, 预填充 / 输出 O = FlashAttn(Q,K,V)]:
+ *   the prompt's own causal softmax attention before any compression, every
+ *   degree still 1 (N = [1]*n, so the log-degree term is 0 and left out):
+ *   o_{h,i} = softmax_{t <= i}(q_{h,i} . k_t * scale) V over rows 0..i of the
+ *   KV head that serves q head h (contiguous groups, G = Hq / Hkv).
+ * q: [B][Hq][n][d]; K, V: [B][Hkv][cap][d] (rows 0..n-1 hold the prompt);
+ * rows: nrows query positions to evaluate (NULL: all n, nrows = n);
+ * out: [B][Hq][nrows][d].
+ */
+void oracle_prefill_attn(const double* q, const double* K, const double* V, int32_t B,
+                         int32_t Hkv, int32_t Hq, int32_t n, int32_t cap, int32_t d,
+                         double scale, const int32_t* rows, int32_t nrows, double* out,
+                         int32_t nthreads)
+{
+    const int32_t G = Hq / Hkv;
+    const long long total = (long long)B * Hq * nrows;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads > 0 ? nthreads : 1)
+    for (long long job = 0; job < total; ++job) {
+        const int32_t r = (int32_t)(job % nrows);
+        const int32_t bh = (int32_t)(job / nrows);
+        const int32_t b = bh / Hq, h = bh % Hq, kv = h / G;
+        const int32_t i = rows ? rows[r] : r;
+        const double* qi = q + ((size_t)bh * n + i) * d;
+        const double* Ku = K + ((size_t)b * Hkv + kv) * cap * d;
+        const double* Vu = V + ((size_t)b * Hkv + kv) * cap * d;
+        double* o = out + ((size_t)bh * nrows + r) * d;
+        for (int32_t e = 0; e < d; ++e) o[e] = 0.0;
+        double* logit = (double*)malloc(sizeof(double) * (size_t)(i + 1));
+        double mx = -INFINITY;
+        for (int32_t t = 0; t <= i; ++t) {
+            double dot = 0.0;
+            for (int32_t e = 0; e < d; ++e) dot += qi[e] * Ku[(size_t)t * d + e];
+            logit[t] = dot * scale;
+            if (logit[t] > mx) mx = logit[t];
+        }
+        double den = 0.0;
+        for (int32_t t = 0; t <= i; ++t) {
+            const double w = exp(logit[t] - mx);
+            den += w;
+            for (int32_t e = 0; e < d; ++e) o[e] += w * Vu[(size_t)t * d + e];
+        }
+        for (int32_t e = 0; e < d; ++e) o[e] /= den;
         free(logit);
     }
 }
