@@ -513,7 +513,7 @@ def run_gpu(args):
                         "avg_call_us": 1e6 * avg_launch_s},
         "roofline": {"bound": "hbm", "achieved": per_launch_bytes / avg_launch_s / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": per_launch_bytes / avg_launch_s / 1e9 / hbm,
-                     "traffic": traffic_record("decode_attn", "bytes_per_launch", w) if kv is None else None, "kernel": "decode_step_logn (append + log-N attention, one kernel)",
+                     "traffic": traffic_record("decode_attn", "bytes_per_launch", w) if kv is None else None, "kernel": "decode_step_logn (append + log-N attention over token splits, then the merge of the splits; one call, two kernels)",
                      "peak_kind": kind, "bytes_per_launch": per_launch_bytes},
         "roofline_csm": {"bound": "hbm", "achieved": csm_gbs, "peak": hbm, "unit": "GB/s", "frac": csm_gbs / hbm,
                          "traffic": traffic_record("csm_compress", "bytes_per_step", w) if kv is None else None, "kernel": "csm_compress",

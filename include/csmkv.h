@@ -375,6 +375,56 @@ typedef struct {
 int csm_decode_run(const csm_decode_loop* loop, int32_t first_step, int32_t steps, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Prefill attention, with the first CSM round fused into it
+ *   [Chelsea §三 算法流程, Algorithm 1: 预填充 O = FlashAttn(Q,K,V), every degree
+ *    N = 1; then, if s >= B + g, the first Chelsea(K,V,N,s,n1,n2,r,c) round]
+ *
+ * prefill_attn: for every sequence b, query head h and prompt position i < s_b,
+ *   out[b][h][i] = softmax_{t <= i}(q[b][h][i] . K[b][h / G][t] * scale) V[b][h / G][t]
+ *   (causal; G = h_q / h_kv query heads per KV head; no log-degree term, since
+ *   every prompt degree is 1). Positions i >= s_b of out are not written.
+ * prefill_attn_csm: the same attention, and, from the same K/V tiles while
+ *   they are on chip, a second cache (K_out, V_out, N_out, len_out, layout
+ *   `cache_out`) holding the prompt after one CSM round with ratio r: exactly
+ *   what csm_compress (the tensor-core kernel) leaves in place on a cache
+ *   whose first s_b rows are the prompt with N = 1 and len = s_b -- sinks, the
+ *   chunks' output rows, remainder and recent window, N and len -- written
+ *   out of place, because later query blocks still read the prompt's rows.
+ *   Units of an outlier head (head_mask[h] = 1), units without a full chunk,
+ *   and every unit when r gives m = 0 get the prompt unchanged (N = 1,
+ *   len = s_b). Rows of the second cache past len_out are not written.
+ *
+ * q: device bf16 [batch][h_q][n][128]; K, V: device, the prompt's rows
+ *   [0, n) of a cache (layout `cache`; bf16, head_dim 128; read only).
+ * n: prompt rows per sequence (0 <= n <= cache->cap); seq_len: device int32
+ *   [batch] with the sequences' own prompt lengths s_b (clamped to [0, n]),
+ *   or NULL (s_b = n for all).
+ * scale: softmax scale; <= 0 -> 1/sqrt(128).
+ * out: device bf16 [batch][h_q][n][128].
+ * cache_out: batch, h_kv, head_dim and dtype as `cache`, cap >= n; K_out,
+ *   V_out, N_out (16-byte aligned) and len_out [batch][h_kv] are device and
+ *   written only. n1, n2 >= 0, 0 <= r <= 0.5 and c == 256 (other c:
+ *   CSMKV_ERR_UNSUPPORTED), as csm_compress.
+ * head_mask: device uint8 [h_kv] or NULL, as csm_compress.
+ * workspace: device, >= prefill_workspace_bytes(), zero-filled once (its
+ *   status word records a bounded wait that ran out: CSMKV_ERR_TIMEOUT).
+ * Returns CSMKV_ERR_UNSUPPORTED for dtypes other than bf16 or head_dim != 128.
+ * Work: one 256-thread CTA per (128-row query block, query head), tcgen05
+ * MMAs with fp32 accumulation in TMEM, bf16 softmax probabilities.
+ * ---------------------------------------------------------------------- */
+size_t prefill_workspace_bytes(void);
+
+int prefill_attn(const void* q, const void* K, const void* V, const csmkv_cache* cache, int32_t n,
+                 const int32_t* seq_len, int32_t h_q, float scale, void* out, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+int prefill_attn_csm(const void* q, const void* K, const void* V, const csmkv_cache* cache, int32_t n,
+                     const int32_t* seq_len, int32_t h_q, float scale, void* out, void* K_out, void* V_out,
+                     int32_t* N_out, int32_t* len_out, const csmkv_cache* cache_out, int32_t n1, int32_t n2,
+                     int32_t c, double r, const uint8_t* head_mask, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/* ------------------------------------------------------------------------
  * Host-side schedule helpers   [Chelsea §三 算法流程, Algorithm 1;
  *                               CentroidKV 分块软匹配 (CSM), 渐进式调度]
  * Pure functions; no device work.

@@ -118,6 +118,10 @@ _SIGS = {
                                               P, SZ, P]),
     "decode_step_logn_paged": (ctypes.c_int, [P, P, P, P, P, P, P, CP, ctypes.POINTER(Pages), I32,
                                               ctypes.c_float, P, P, SZ, P]),
+    "prefill_workspace_bytes": (SZ, []),
+    "prefill_attn": (ctypes.c_int, [P, P, P, CP, I32, P, I32, ctypes.c_float, P, P, SZ, P]),
+    "prefill_attn_csm": (ctypes.c_int, [P, P, P, CP, I32, P, I32, ctypes.c_float, P, P, P, P, P, CP, I32, I32,
+                                        I32, F64, P, P, SZ, P]),
     "csm_budget": (F64, [I64, F64, I64]),
     "csm_should_trigger": (ctypes.c_int, [I64, F64, I32]),
     "csm_ratio": (F64, [I32, F64, F64, F64]),
@@ -356,6 +360,32 @@ def decode_step_logn_paged(q, k_new, v_new, kv, length, out, workspace, scale=No
 
 
 # ---------------------------------------------------------------- host helpers
+# ---------------------------------------------------------------- prefill
+def prefill_workspace_bytes() -> int:
+    return int(load().prefill_workspace_bytes())
+
+
+def prefill_attn(q, K, V, n, out, workspace, seq_len=None, scale=None, stream=None):
+    """Causal prefill attention over the prompt rows [0, n) of the cache (K, V).
+    q, out: [batch, h_q, n, 128]; seq_len: optional int32 [batch] prompt lengths."""
+    cache = cache_desc(K)
+    rc = load().prefill_attn(_ptr(q), _ptr(K), _ptr(V), ctypes.byref(cache), int(n), _ptr(seq_len), q.shape[1],
+                             float(scale or 0.0), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("prefill_attn", rc)
+
+
+def prefill_attn_csm(q, K, V, n, out, K_out, V_out, N_out, len_out, n1, n2, c, r, workspace, seq_len=None,
+                     head_mask=None, scale=None, stream=None):
+    """prefill_attn plus the prompt's first CSM round (ratio r) written to a second cache."""
+    cache = cache_desc(K)
+    cache_out = cache_desc(K_out)
+    rc = load().prefill_attn_csm(_ptr(q), _ptr(K), _ptr(V), ctypes.byref(cache), int(n), _ptr(seq_len), q.shape[1],
+                                 float(scale or 0.0), _ptr(out), _ptr(K_out), _ptr(V_out), _ptr(N_out),
+                                 _ptr(len_out), ctypes.byref(cache_out), n1, n2, c, float(r), _ptr(head_mask),
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("prefill_attn_csm", rc)
+
+
 def csm_budget(n, R, Gamma) -> float:
     return float(load().csm_budget(int(n), float(R), int(Gamma)))
 

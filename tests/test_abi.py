@@ -39,7 +39,8 @@ def test_every_declared_symbol_is_exported(lib):
         "csm_decode_run", "csm_budget", "csm_chunks_to_budget", "csm_should_trigger",
         "csm_ratio", "csm_edges_per_chunk", "csm_num_chunks", "csm_len_after", "csmkv_device_status",
         "csmkv_clear_status", "csmkv_status_str", "csm_append_paged", "csm_compress_paged",
-        "decode_attn_logn_paged", "decode_step_logn_paged"]), names
+        "decode_attn_logn_paged", "decode_step_logn_paged", "prefill_workspace_bytes", "prefill_attn",
+        "prefill_attn_csm"]), names
     raw = ctypes.CDLL(_build.OUT)
     for n in names:
         assert hasattr(raw, n), f"{n} declared in csmkv.h but not exported"
@@ -138,6 +139,36 @@ def test_attention_argument_errors_without_gpu(lib):
     assert call(h_q=18) == 8         # bf16 group of 9 query heads is not covered
     assert call(cache=_cache(head_dim=96)) == 8
     assert lib.csm_append(None, None, None, None, ctypes.byref(c), None, None, None, None, 0, None) == 1
+
+
+def test_prefill_argument_errors_without_gpu(lib):
+    P = ctypes.c_void_p
+    c = _cache()  # bf16, head_dim 128
+
+    def attn(h_q=8, n=100, ptr=4096, cache=c, ws=1 << 16, wsb=256, scale=0.0):
+        return lib.prefill_attn(P(ptr), P(ptr), P(ptr), ctypes.byref(cache), n, None, h_q, scale, P(ptr), P(ws), wsb,
+                                None)
+    assert lib.prefill_workspace_bytes() >= 4
+    assert attn(h_q=3) == 1          # not a multiple of h_kv
+    assert attn(n=-1) == 1
+    assert attn(n=c.cap + 1) == 1    # the prompt must fit in the cache
+    assert attn(scale=float("nan")) == 1
+    assert attn(cache=_cache(head_dim=64)) == 8
+    assert attn(cache=_cache(dtype=1)) == 8
+    assert attn(ptr=4104) == 3
+    assert attn(wsb=0) == 5
+    assert attn(ws=0) == 5
+
+    def fused(n=100, cap_out=None, c_=256, r=0.5, N_out=4096, n1=16):
+        co = _cache() if cap_out is None else _cache(cap=cap_out)
+        return lib.prefill_attn_csm(P(4096), P(4096), P(4096), ctypes.byref(c), n, None, 8, 0.0, P(4096), P(4096),
+                                    P(4096), P(N_out), P(4096), ctypes.byref(co), n1, 64, c_, r, None, P(1 << 16),
+                                    256, None)
+    assert fused(cap_out=64) == 1    # the second cache must hold the prompt
+    assert fused(r=0.6) == 1
+    assert fused(n1=-1) == 1
+    assert fused(N_out=0) == 1
+    assert fused(c_=128) == 8        # the fused round covers c == 256 only
 
 
 def test_no_workspace_attention_checks_arguments_before_touching_the_gpu(lib):
