@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 break;
             }
             tc_fence_after();
-            if (rescale) {
+            if (__any_sync(0xffffffffu, rescale)) {  // the TMEM accesses are warp-wide; factor is 1 elsewhere
                 l *= factor;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {

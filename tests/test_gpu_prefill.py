@@ -75,6 +75,21 @@ def test_prefill_attention_matches_oracle(batch, h_kv, G, n, seq_len):
     assert torch.equal(out, out2), "repeated calls differ"
 
 
+@pytest.mark.parametrize("grow", [6.0, 0.1])
+def test_prefill_attention_when_scores_grow_or_shrink(grow):
+    """Keys past row 200 scaled up (the running row max grows by far more than 2^8, so O
+    is rescaled in TMEM mid-row) or down (no rescale)."""
+    n = 600
+    q, K, V, lens, sl = _prompt(11, 1, 2, 2, n, 608)
+    K[:, :, 200:n] = (K[:, :, 200:n].float() * grow).to(torch.bfloat16)
+    out = torch.full((1, 4, n, D), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    ws = B.new_workspace(B.prefill_workspace_bytes(), "cuda")
+    B.prefill_attn(q, K, V, n, out, ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0
+    _attention_check(q, K, V, lens, out, n)
+
+
 def _standalone_round(K, V, lens, n1, n2, c, r, head_mask):
     """The prompt as a cache with N = 1 and len = s, compressed in place by csm_compress."""
     Ks, Vs = K.clone(), V.clone()
