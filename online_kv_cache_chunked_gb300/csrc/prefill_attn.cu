@@ -108,6 +108,24 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const float (
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 128 consecutive 32-bit columns (thread i: lane base + i), completed
+// (tcgen05.wait::ld) inside the same statement, so no use can move above the wait.
+__device__ __forceinline__ void tmem_ld_32x32b_x128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 2^x on the MUFU unit (ex2.approx, flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Bounded mbarrier wait by a whole warp, with one outcome for all its lanes (the
 // warp goes on to .sync.aligned tcgen05 instructions).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
@@ -274,27 +292,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ok = warp_wait(&br.s_full[st], (t >> 1) & 1, deadline);
             if (!__all_sync(0xffffffffu, ok && !*err)) break;
             tc_fence_after();
+            uint32_t sv[128];  // the row's 128 scores of this tile, one pass over TMEM
+            tmem_ld_32x32b_x128(tS(st) + lo, sv);
             const int k0 = p.off + t * kPfTile;
             const int jlo = max(0, -k0), jhi = min(kPfTile - 1, qrow - k0);  // visible columns (inclusive)
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float v[32];
-                tmem_ld_32x32b_x32(tS(st) + lo + (uint32_t)(cb * 32), v);
+            if (__any_sync(0xffffffffu, jlo > 0 || jhi < kPfTile - 1)) {  // first or diagonal tile
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = cb * 32 + e;
-                    if (j >= jlo && j <= jhi) mx = fmaxf(mx, v[e]);
-                }
+                for (int j = 0; j < kPfTile; ++j)
+                    if (j < jlo || j > jhi) sv[j] = 0xff800000u;  // -inf: weight 0, never the max
             }
-            const float m_tile = mx * p.scale_log2;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < kPfTile; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sv[j]));
+            const float m_tile = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
             float m_use = m_run, factor = 1.f;
             bool rescale = false;
             if (m_tile > m_run + kPfLazy) {
                 m_use = m_tile;
                 if (m_run != -INFINITY) {
                     rescale = true;
-                    factor = exp2f(m_run - m_tile);
+                    factor = ex2_approx(m_run - m_tile);
                 }
             }
             // P's buffer and O are free once the previous tile's P V has completed
@@ -315,27 +332,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 tmem_st_wait();
             }
-            const bool live = m_use != -INFINITY;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float v[32];
-                tmem_ld_32x32b_x32(tS(st) + lo + (uint32_t)(cb * 32), v);
-                uint32_t pk[16];
+            const float mneg = m_use == -INFINITY ? 0.f : -m_use;  // a row with nothing visible: all 0
+            const float sl = p.scale_log2;
+            float ls[2] = {0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int j = cb * 32 + e;
-                    const float p0 = (live && j >= jlo && j <= jhi) ? exp2f(fmaf(v[e], p.scale_log2, -m_use)) : 0.f;
-                    const float p1 =
-                        (live && j + 1 >= jlo && j + 1 <= jhi) ? exp2f(fmaf(v[e + 1], p.scale_log2, -m_use)) : 0.f;
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    l += bf16lo(w) + bf16hi(w);  // the row sum of the P the MMA multiplies
-                    pk[e >> 1] = w;
+            for (int k = 0; k < 16; ++k) {  // 8 columns = one 16-byte piece of the row's P
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[8 * k + 2 * e]), sl, mneg));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[8 * k + 2 * e + 1]), sl, mneg));
+                    ls[e & 1] += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)  // columns cb*32 + 8k .. +7 -> piece 4 cb + k of the row
-                    *reinterpret_cast<uint4*>(sP + tile_piece(r, cb * 4 + k)) =
-                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                *reinterpret_cast<uint4*>(sP + tile_piece(r, k)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            l += ls[0] + ls[1];
             tc_fence_before();
             fence_proxy_async_smem();  // P (generic-proxy writes) before the tensor core reads it
             __syncwarp();
