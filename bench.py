@@ -483,6 +483,7 @@ def run_gpu(args):
     clocks = clk.summary()
     if rank != 0:
         return 0
+    prefill = prefill_measure(w, d, K0, V0, L0, args) if kv is None and not args.no_prefill else None
     hbm, kind = peaks()
     attn_gbs = agg["attn_bytes"] / agg["attn_s"] / 1e9
     per_launch_bytes = attn_bytes_step / w.steps
@@ -525,9 +526,11 @@ def run_gpu(args):
                             "gbs": csm_stats[k][1] / (round_ms[k] / 1e3) / 1e9}
                            for k, rd in enumerate(rounds)]},
         "e2e": e2e,
-        # per decode step: the fused append + attention kernel (+ its prologue beyond 2048
-        # units) and the L2 eviction read when enabled; per round: prologue + main kernel
-        "gpu_launches": args.steps * (2 * len(rounds) + ((1 if w.batch * w.h_kv <= 2048 else 2)
+        "prefill": prefill,
+        # per decode step: the split kernel and the merge kernel (+ a planning prologue
+        # beyond 512 units) and the L2 eviction read when enabled; per round: prologue +
+        # main kernel
+        "gpu_launches": args.steps * (2 * len(rounds) + ((2 if w.batch * w.h_kv <= 512 else 3)
                                                           + (1 if flush is not None else 0)) * w.steps),
         "clocks": clocks,
     }
@@ -538,6 +541,88 @@ def run_gpu(args):
                                 "sample": cpu["sample"], "seconds": cpu["seconds"], "decode": cpu.get("decode")}
     print(json.dumps(line))
     return 0
+
+
+def prefill_measure(w, d, K0, V0, L0, args, reps=3):
+    """The prompt's attention with the first CSM round fused into it, on one layer of the
+    workload (its sequences and all their heads): prefill_attn_csm (attention, and the
+    compressed prompt written to a second cache), prefill_attn (attention alone) and the
+    standalone round on the same prompt, timed with CUDA events; FLOPs are the causal
+    attention's 4 d sum_i (i + 1) per query head."""
+    import torch
+
+    from online_kv_cache_chunked_gb300 import binding as B
+
+    if w.dtype != "bf16" or w.d != 128 or w.c != 256:
+        return {"unavailable": "the fused prefill kernel covers bf16, head_dim 128, c = 256"}
+    rows = slice(0, w.seqs)  # layer 0 of every sequence
+    K, V = K0[rows].contiguous(), V0[rows].contiguous()
+    lens = L0[rows][:, 0].to(torch.int32).contiguous()
+    n = int(lens.max())
+    g = torch.Generator(device=K.device).manual_seed(1234)
+    q = torch.randn(w.seqs, w.h_q, n, w.d, device=K.device, generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    Ko, Vo = torch.empty_like(K), torch.empty_like(V)
+    No = torch.empty(K.shape[:3], dtype=torch.int32, device=K.device)
+    Lo = torch.empty(K.shape[:2], dtype=torch.int32, device=K.device)
+    ws = B.new_workspace(B.prefill_workspace_bytes(), K.device)
+    hm = d["head_mask"]
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        return float(np.median(ts))
+
+    t_fused = timed(lambda: B.prefill_attn_csm(q, K, V, n, out, Ko, Vo, No, Lo, w.n1, w.n2, w.c, w.r_init, ws,
+                                               seq_len=lens, head_mask=hm))
+    t_attn = timed(lambda: B.prefill_attn(q, K, V, n, out, ws, seq_len=lens))
+    st = B.csmkv_device_status(ws)
+    # the same round by csm_compress on a copy of the prompt (N = 1, len = s)
+    Kc, Vc = K.clone(), V.clone()
+    Nc = torch.ones_like(No)
+    Lc = lens[:, None].expand(-1, w.h_kv).contiguous()
+    wsc = B.new_workspace(B.csm_workspace_bytes(B.cache_desc(Kc), w.n1, w.n2, w.c), K.device)
+
+    def restore():
+        Kc.copy_(K)
+        Vc.copy_(V)
+        Nc.fill_(1)
+        Lc.copy_(lens[:, None].expand(-1, w.h_kv))
+    t_restore = timed(restore)
+    t_round = timed(lambda: (restore(), B.csm_compress(Kc, Vc, Nc, Lc, w.n1, w.n2, w.c, w.r_init, head_mask=hm,
+                                                       workspace=wsc))) - t_restore
+    same = bool(torch.equal(Lo, Lc))
+    if same:
+        for u in range(w.seqs):
+            for h in range(w.h_kv):
+                s_ = int(Lc[u, h])
+                same = (same and torch.equal(Ko[u, h, :s_], Kc[u, h, :s_]) and torch.equal(Vo[u, h, :s_], Vc[u, h, :s_])
+                        and torch.equal(No[u, h, :s_], Nc[u, h, :s_]))
+    flops = 4.0 * w.d * w.h_q * float(sum(int(x) * (int(x) + 1) / 2 for x in lens.tolist()))
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(pk.get("bf16_tflops", 1900.0))
+    tf = flops / t_fused / 1e12
+    del q, out, Ko, Vo, Kc, Vc
+    torch.cuda.empty_cache()
+    return {"workload": f"layer 0 of {w.name}: {w.seqs} sequence(s) of up to {n} prompt rows, {w.h_q} query / "
+                        f"{w.h_kv} KV heads, first round r = {w.r_init}",
+            "value": tf, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": "measured (cuBLAS bf16 burst)" if pk else "fallback",
+                         "kernel": "prefill_attn_csm (tcgen05 QK^T and PV, TMEM accumulators)"},
+            "ms_fused": t_fused * 1e3, "ms_attention_only": t_attn * 1e3,
+            "attention_only_tflops": flops / t_attn / 1e12,
+            "fused_round_extra_ms": (t_fused - t_attn) * 1e3, "standalone_round_ms": t_round * 1e3,
+            "second_cache_equals_standalone_round": same, "device_status": st}
 
 
 def e2e_measure_paged(w, d, kv, kv0, L0, p, rounds, args):
@@ -739,6 +824,8 @@ def main():
                     help="run on a paged (block-table) copy of the cache: pages of --page-rows rows at scattered "
                          "pool pages")
     ap.add_argument("--page-rows", type=int, default=256)
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the fused prefill attention + first round leg")
     ap.add_argument("--e2e-groups", type=int, default=32,
                     help="the end-to-end leg pipelines uploads, compression and downloads over this many "
                          "groups of cache rows")
