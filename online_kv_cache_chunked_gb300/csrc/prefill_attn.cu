@@ -8,7 +8,8 @@
 // n1 + 256 j) is exactly two key tiles, and query block i and key tile i cover the
 // same rows (the diagonal, where the causal mask cuts).
 // Warp roles during the attention:
-//   warp 0     TMA: the query block once, then K and V tiles through a 2-stage ring;
+//   warp 0     TMA (two lanes): the query block once, then K tiles and V tiles through
+//              2-stage rings released separately (K after Q K^T, V after P V);
 //   warp 1     tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
 //              (128 columns each), and O += P V into a third; the warp's lanes zero
 //              V rows past the prompt before they are used (they may hold anything);
@@ -62,7 +63,7 @@ struct PfParams {
 
 struct alignas(8) PfBars {
     uint64_t q_full;
-    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full, pv_done, csm_mma, drain;
     uint32_t tmem;
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int k = 0; k < 2; ++k) {
             mbar_init(&br.k_full[k], 1);
             mbar_init(&br.v_full[k], 1);
-            mbar_init(&br.kv_empty[k], 1);
+            mbar_init(&br.k_empty[k], 1);
+            mbar_init(&br.v_empty[k], 1);
             mbar_init(&br.s_full[k], 1);
             mbar_init(&br.s_empty[k], 4);
         }
@@ -201,28 +203,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         record_status(status, CSMKV_ERR_TIMEOUT);
         *err = 1;
     };
-    int last_load[2] = {-1, -1};  // warp 0 lane 0: last tile loaded into each stage
+    int last_load[2] = {-1, -1};  // warp 0 lanes 0 (K) and 1 (V): last tile loaded into each stage
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
-        if (lane == 0) {
-            mbar_expect_tx(&br.q_full, kPfTileBytes);
-            tma_load_3d(sQ, &tmQ, &br.q_full, 0, row0, qh);
-            tma_load_3d(sQ + 16384, &tmQ, &br.q_full, 64, row0, qh);
+        // lane 0: the query block, then K tiles (a stage is free once S = Q K^T of the tile
+        // two before has completed); lane 1: V tiles (free once that tile's P V has)
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            if (is_k) {
+                mbar_expect_tx(&br.q_full, kPfTileBytes);
+                tma_load_3d(sQ, &tmQ, &br.q_full, 0, row0, qh);
+                tma_load_3d(sQ + 16384, &tmQ, &br.q_full, 64, row0, qh);
+            }
+            uint64_t* const empty = is_k ? br.k_empty : br.v_empty;
+            uint64_t* const full = is_k ? br.k_full : br.v_full;
+            const CUtensorMap* const map = is_k ? &tmK : &tmV;
             for (int t = 0; t <= i; ++t) {
                 const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&br.kv_empty[st], ((t >> 1) - 1) & 1, deadline)) {
+                if (t >= 2 && !mbar_wait(&empty[st], ((t >> 1) - 1) & 1, deadline)) {
                     fail();
                     break;
                 }
                 if (*err) break;
                 const int r = p.off + t * kPfTile;
-                mbar_expect_tx(&br.k_full[st], kPfTileBytes);
-                tma_load_3d(sK(st), &tmK, &br.k_full[st], 0, r, u);
-                tma_load_3d(sK(st) + 16384, &tmK, &br.k_full[st], 64, r, u);
-                mbar_expect_tx(&br.v_full[st], kPfTileBytes);
-                tma_load_3d(sV(st), &tmV, &br.v_full[st], 0, r, u);
-                tma_load_3d(sV(st) + 16384, &tmV, &br.v_full[st], 64, r, u);
+                uint8_t* const dst = is_k ? sK(st) : sV(st);
+                mbar_expect_tx(&full[st], kPfTileBytes);
+                tma_load_3d(dst, map, &full[st], 0, r, u);
+                tma_load_3d(dst + 16384, map, &full[st], 64, r, u);
                 last_load[st] = t;
             }
         }
@@ -241,6 +249,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_mma_bf16(tS(st), ad, bd, idS, ks > 0 ? 1u : 0u);
             }
             tc_commit(&br.s_full[st]);
+            tc_commit(&br.k_empty[st]);
         };
         bool ok = warp_wait(&br.q_full, 0, deadline) && warp_wait(&br.k_full[0], 0, deadline);
         if (ok && lane == 0) issue_S(0);
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_mma_bf16(tO, ad, bd, idPV, (t > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc_commit(&br.pv_done);
-                tc_commit(&br.kv_empty[st]);
+                tc_commit(&br.v_empty[st]);
             }
             __syncwarp();
         }
@@ -503,14 +512,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_commit(&br.drain);
         (void)mbar_wait(&br.drain, 0, globaltimer() + (uint64_t)p.timeout_ns);
     }
-    if (tid == 0) {  // after a timeout, loads still in flight land before the CTA leaves
+    if (tid < 2) {  // after a timeout, loads still in flight land before the CTA leaves
         const uint64_t dl = globaltimer() + (uint64_t)p.timeout_ns;
-        (void)mbar_wait(&br.q_full, 0, dl);
+        if (tid == 0) (void)mbar_wait(&br.q_full, 0, dl);
+        uint64_t* const full = tid == 0 ? br.k_full : br.v_full;
         for (int st = 0; st < 2; ++st)
-            if (last_load[st] >= 0) {
-                (void)mbar_wait(&br.k_full[st], (last_load[st] >> 1) & 1, dl);
-                (void)mbar_wait(&br.v_full[st], (last_load[st] >> 1) & 1, dl);
-            }
+            if (last_load[st] >= 0) (void)mbar_wait(&full[st], (last_load[st] >> 1) & 1, dl);
     }
     tc_fence_before();
     __syncthreads();
