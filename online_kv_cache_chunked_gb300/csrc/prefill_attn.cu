@@ -35,12 +35,13 @@ constexpr int kPfTile = 128;      // query rows per block = key rows per tile
 constexpr int kPfTileBytes = 32768;  // 128 rows x 128 bf16 (two 64-column boxes)
 constexpr float kPfLazy = 8.0f;   // log2 of the growth of the row max tolerated before a rescale
 
-constexpr int kOffQ = 0;                      // query block, later the CSM parity slot (with P)
-constexpr int kOffP = kOffQ + kPfTileBytes;   // P, the A operand of O += P V
-constexpr int kOffK0 = kOffP + kPfTileBytes;  // ring: K0 V0 K1 V1
-constexpr int kOffTables = kOffK0 + 4 * kPfTileBytes;
+constexpr int kOffQ = 0;                          // query block, later the CSM parity slot (with P0)
+constexpr int kOffP = kOffQ + kPfTileBytes;       // P0, P1: the A operand of O += P V, two buffers
+constexpr int kOffK0 = kOffP + 2 * kPfTileBytes;  // rings: K0 V0 K1 V1
+constexpr int kOffTables = kOffP + kPfTileBytes;  // CSM tables and prompt degrees in P1 (after the attention)
 constexpr int kOffOnes = kOffTables + (int)sizeof(CsmTables);
-constexpr int kOffBars = kOffOnes + 256 * 4;
+constexpr int kOffBars = kOffK0 + 4 * kPfTileBytes;
+static_assert(kOffOnes + 256 * 4 <= kOffK0, "CSM tables fit in the second P buffer");
 
 struct PfParams {
     const int32_t* seq_len;  // [batch] prompt rows per sequence, or null (all n)
@@ -65,7 +66,7 @@ struct alignas(8) PfBars {
     uint64_t q_full;
     uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
     uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, pv_done, csm_mma, drain;
+    uint64_t p_full[2], pv_done[2], csm_mma, drain;
     uint32_t tmem;
     int32_t err;
 };
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* const sb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* const sQ = sb + kOffQ;
-    uint8_t* const sP = sb + kOffP;
+    auto sP = [&](int pb) { return sb + kOffP + pb * kPfTileBytes; };
     CsmTables& sm = *reinterpret_cast<CsmTables*>(sb + kOffTables);
     int32_t* const ones = reinterpret_cast<int32_t*>(sb + kOffOnes);
     PfBars& br = *reinterpret_cast<PfBars*>(sb + kOffBars);
@@ -178,8 +179,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&br.s_full[k], 1);
             mbar_init(&br.s_empty[k], 4);
         }
-        mbar_init(&br.p_full, 4);
-        mbar_init(&br.pv_done, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&br.p_full[k], 4);
+            mbar_init(&br.pv_done[k], 1);
+        }
         mbar_init(&br.csm_mma, 1);
         mbar_init(&br.drain, 1);
         br.err = 0;
@@ -251,41 +254,65 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_commit(&br.s_full[st]);
             tc_commit(&br.k_empty[st]);
         };
-        bool ok = warp_wait(&br.q_full, 0, deadline) && warp_wait(&br.k_full[0], 0, deadline);
-        if (ok && lane == 0) issue_S(0);
-        for (int t = 0; ok && t <= i; ++t) {
-            if (t + 1 <= i) {
-                const int t1 = t + 1, st1 = t1 & 1;
-                ok = warp_wait(&br.k_full[st1], (t1 >> 1) & 1, deadline) &&
-                     (t1 < 2 || warp_wait(&br.s_empty[st1], ((t1 >> 1) - 1) & 1, deadline));
-                if (!__all_sync(0xffffffffu, ok && !*err)) break;
-                if (lane == 0) issue_S(t1);
+        // Issue order follows readiness: S = Q K^T of tile ns as soon as its K has landed
+        // and its S buffer has been read (so S runs up to two tiles ahead of the softmax),
+        // P V of tile np as soon as its P and V are in shared memory. Tests are
+        // non-blocking and taken by the whole warp, so lane 0 never waits on one
+        // barrier while the other operation is ready.
+        bool ok = warp_wait(&br.q_full, 0, deadline);
+        int ns = 0, np = 0;  // next S and next P V to issue
+        while (ok && np <= i) {
+            if (!__all_sync(0xffffffffu, !*err)) {
+                ok = false;
+                break;
             }
-            const int st = t & 1;
-            ok = warp_wait(&br.p_full, t & 1, deadline) && warp_wait(&br.v_full[st], (t >> 1) & 1, deadline);
-            if (!__all_sync(0xffffffffu, ok && !*err)) break;
-            const int rt = p.off + t * kPfTile;
-            if (rt + kPfTile > s) {  // rows at or past the prompt's end: their V may hold anything
-                const int z0 = s - rt;  // first such row of the tile (> 0: the tile holds row s - 1)
-                for (int x = lane; x < (kPfTile - z0) * 16; x += 32) {
-                    const int r = z0 + (x >> 4), k = x & 15;
-                    *reinterpret_cast<uint4*>(sV(st) + tile_piece(r, k)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
-                tc_fence_after();
+            bool did = false;
+            if (np < ns) {
+                const int st = np & 1;
+                const bool ready = __all_sync(0xffffffffu, mbar_test(&br.p_full[st], (np >> 1) & 1) &&
+                                                               mbar_test(&br.v_full[st], (np >> 1) & 1));
+                if (ready) {
+                    const int rt = p.off + np * kPfTile;
+                    if (rt + kPfTile > s) {  // rows at or past the prompt's end: their V may hold anything
+                        const int z0 = s - rt;  // first such row of the tile (> 0: the tile holds row s - 1)
+                        for (int x = lane; x < (kPfTile - z0) * 16; x += 32) {
+                            const int r = z0 + (x >> 4), k = x & 15;
+                            *reinterpret_cast<uint4*>(sV(st) + tile_piece(r, k)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    if (lane == 0) {
+                        tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sP + (ks >> 2) * 16384 + (ks & 3) * 32));
-                    const uint64_t bd = smem_desc_mn_sw128(smem_u32(sV(st) + ks * 2048), 16384);
-                    tc_mma_bf16(tO, ad, bd, idPV, (t > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step
+                            const uint64_t ad = smem_desc_sw128(smem_u32(sP(st) + (ks >> 2) * 16384 + (ks & 3) * 32));
+                            const uint64_t bd = smem_desc_mn_sw128(smem_u32(sV(st) + ks * 2048), 16384);
+                            tc_mma_bf16(tO, ad, bd, idPV, (np > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&br.pv_done[st]);
+                        tc_commit(&br.v_empty[st]);
+                    }
+                    __syncwarp();
+                    ++np;
+                    did = true;
                 }
-                tc_commit(&br.pv_done);
-                tc_commit(&br.v_empty[st]);
             }
-            __syncwarp();
+            if (ns <= i) {
+                const int st = ns & 1;
+                const bool ready = __all_sync(0xffffffffu, mbar_test(&br.k_full[st], (ns >> 1) & 1) &&
+                                                               (ns < 2 || mbar_test(&br.s_empty[st], ((ns >> 1) - 1) & 1)));
+                if (ready) {
+                    if (lane == 0) issue_S(ns);
+                    __syncwarp();
+                    ++ns;
+                    did = true;
+                }
+            }
+            if (!did) {
+                if (globaltimer() > deadline) ok = false;
+                __nanosleep(20);  // leave the issue slots to the softmax warp sharing this sub-partition
+            }
         }
         if (!ok && lane == 0) fail();
     } else if (warp >= 4) {
@@ -303,6 +330,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_fence_after();
             uint32_t sv[128];  // the row's 128 scores of this tile, one pass over TMEM
             tmem_ld_32x32b_x128(tS(st) + lo, sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&br.s_empty[st]);  // S buffer st may take the tile after next
             const int k0 = p.off + t * kPfTile;
             const int jlo = max(0, -k0), jhi = min(kPfTile - 1, qrow - k0);  // visible columns (inclusive)
             if (__any_sync(0xffffffffu, jlo > 0 || jhi < kPfTile - 1)) {  // first or diagonal tile
@@ -323,13 +353,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     factor = ex2_approx(m_run - m_tile);
                 }
             }
-            // P's buffer and O are free once the previous tile's P V has completed
-            if (t >= 1 && !warp_wait(&br.pv_done, (t - 1) & 1, deadline)) {
+            // P buffer t & 1 is free once tile t - 2's P V has completed; O may be rescaled
+            // once tile t - 1's has (P V of tile t cannot start before this P is written)
+            if (t >= 2 && !warp_wait(&br.pv_done[st], ((t - 2) >> 1) & 1, deadline)) {
+                ok = false;
+                break;
+            }
+            const bool any_rescale = __any_sync(0xffffffffu, rescale);
+            if (any_rescale && t >= 1 && !warp_wait(&br.pv_done[st ^ 1], ((t - 1) >> 1) & 1, deadline)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            if (__any_sync(0xffffffffu, rescale)) {  // the TMEM accesses are warp-wide; factor is 1 elsewhere
+            if (any_rescale) {  // the TMEM accesses are warp-wide; factor is 1 elsewhere
                 l *= factor;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
@@ -354,19 +390,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     ls[e & 1] += p0 + p1;
                     w[e] = pack_bf16x2(p0, p1);
                 }
-                *reinterpret_cast<uint4*>(sP + tile_piece(r, k)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(sP(st) + tile_piece(r, k)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             l += ls[0] + ls[1];
             tc_fence_before();
             fence_proxy_async_smem();  // P (generic-proxy writes) before the tensor core reads it
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&br.s_empty[st]);
-                mbar_arrive(&br.p_full);
-            }
+            if (lane == 0) mbar_arrive(&br.p_full[st]);
             m_run = m_use;
         }
-        if (ok) ok = __all_sync(0xffffffffu, !*err) && warp_wait(&br.pv_done, i & 1, deadline);
+        if (ok) ok = __all_sync(0xffffffffu, !*err) && warp_wait(&br.pv_done[i & 1], (i >> 1) & 1, deadline);
         if (ok) {
             tc_fence_after();
             const bool valid = qrow >= 0 && qrow < s;
