@@ -128,6 +128,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 32 lanes x 64 consecutive 32-bit columns from r[0..63] (thread i: lane base + i),
+// completed (tcgen05.wait::st) inside the same statement.
+__device__ __forceinline__ void tmem_st_32x32b_x64(uint32_t taddr, const uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A (M rows in TMEM lanes, two 16-bit
+// elements per 32-bit column along K) is read from tensor memory.
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Bounded mbarrier wait by a whole warp, with one outcome for all its lanes (the
 // warp goes on to .sync.aligned tcgen05 instructions).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
@@ -286,9 +308,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step
-                            const uint64_t ad = smem_desc_sw128(smem_u32(sP(st) + (ks >> 2) * 16384 + (ks & 3) * 32));
                             const uint64_t bd = smem_desc_mn_sw128(smem_u32(sV(st) + ks * 2048), 16384);
-                            tc_mma_bf16(tO, ad, bd, idPV, (np > 0 || ks > 0) ? 1u : 0u);
+                            tc_mma_bf16_ta(tO, tS(st) + (uint32_t)(ks * 8), bd, idPV, (np > 0 || ks > 0) ? 1u : 0u);
                         }
                         tc_commit(&br.pv_done[st]);
                         tc_commit(&br.v_empty[st]);
@@ -301,7 +322,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (ns <= i) {
                 const int st = ns & 1;
                 const bool ready = __all_sync(0xffffffffu, mbar_test(&br.k_full[st], (ns >> 1) & 1) &&
-                                                               (ns < 2 || mbar_test(&br.s_empty[st], ((ns >> 1) - 1) & 1)));
+                                                               (ns < 2 || np >= ns - 1));
                 if (ready) {
                     if (lane == 0) issue_S(ns);
                     __syncwarp();
@@ -381,20 +402,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const float sl = p.scale_log2;
             float ls[2] = {0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {  // 8 columns = one 16-byte piece of the row's P
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[8 * k + 2 * e]), sl, mneg));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[8 * k + 2 * e + 1]), sl, mneg));
-                    ls[e & 1] += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(sP(st) + tile_piece(r, k)) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int k = 0; k < 64; ++k) {  // pair k of the row's P, packed in place (sv[k] is free)
+                const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * k]), sl, mneg));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * k + 1]), sl, mneg));
+                ls[k & 1] += p0 + p1;
+                sv[k] = pack_bf16x2(p0, p1);
             }
             l += ls[0] + ls[1];
+            // P into the S buffer's first 64 columns: the A operand of P V, read from TMEM
+            tmem_st_32x32b_x64(tS(st) + lo, sv);
             tc_fence_before();
-            fence_proxy_async_smem();  // P (generic-proxy writes) before the tensor core reads it
             __syncwarp();
             if (lane == 0) mbar_arrive(&br.p_full[st]);
             m_run = m_use;
