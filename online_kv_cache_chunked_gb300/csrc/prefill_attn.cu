@@ -10,14 +10,16 @@
 // Warp roles during the attention:
 //   warp 0     TMA (two lanes): the query block once, then K tiles and V tiles through
 //              2-stage rings released separately (K after Q K^T, V after P V);
-//   warp 1     tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
-//              (128 columns each), and O += P V into a third; the warp's lanes zero
+//   warp 1     tcgen05.mma from one thread, by readiness: S = Q K^T into one of two
+//              TMEM buffers (128 columns each) up to two tiles ahead of the softmax, and
+//              O += P V into a third, P read from tensor memory; the warp's lanes zero
 //              V rows past the prompt before they are used (they may hold anything);
-//   warps 4-7  the online softmax, one thread per query row (its TMEM lane): row max,
-//              P = 2^(x - m) as bf16 into shared memory in the A-operand layout, row
-//              sums; O is rescaled in TMEM only when the row max has grown by more
-//              than 2^8 since the last rescale (until then P <= 2^8, exact in bf16's
-//              range), and divided by the row sum at the end.
+//   warps 4-7  the online softmax, one thread per query row (its TMEM lane): one
+//              128-column load of the row's scores, row max, P = 2^(x - m) packed as
+//              bf16 pairs and stored over the first 64 columns of the same S buffer
+//              (the A operand of P V), row sums; O is rescaled in TMEM only when the row
+//              max has grown by more than 2^8 since the last rescale (until then
+//              P <= 2^8, exact in bf16's range), and divided by the row sum at the end.
 // The degrees of a prompt are all 1, so there is no log-degree term here.
 // Cache output, by the CTA of query head h with h mod G == 0 of each KV head:
 // when its diagonal tile is the second tile of chunk j it runs the chunk's CSM
@@ -36,9 +38,9 @@ constexpr int kPfTileBytes = 32768;  // 128 rows x 128 bf16 (two 64-column boxes
 constexpr float kPfLazy = 8.0f;   // log2 of the growth of the row max tolerated before a rescale
 
 constexpr int kOffQ = 0;                          // query block, later the CSM parity slot (with P0)
-constexpr int kOffP = kOffQ + kPfTileBytes;       // P0, P1: the A operand of O += P V, two buffers
+constexpr int kOffP = kOffQ + kPfTileBytes;       // the fused round's: with the query block, its parity slot,
 constexpr int kOffK0 = kOffP + 2 * kPfTileBytes;  // rings: K0 V0 K1 V1
-constexpr int kOffTables = kOffP + kPfTileBytes;  // CSM tables and prompt degrees in P1 (after the attention)
+constexpr int kOffTables = kOffP + kPfTileBytes;  // then its tables and the prompt degrees
 constexpr int kOffOnes = kOffTables + (int)sizeof(CsmTables);
 constexpr int kOffBars = kOffK0 + 4 * kPfTileBytes;
 static_assert(kOffOnes + 256 * 4 <= kOffK0, "CSM tables fit in the second P buffer");
@@ -169,7 +171,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* const sb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* const sQ = sb + kOffQ;
-    auto sP = [&](int pb) { return sb + kOffP + pb * kPfTileBytes; };
     CsmTables& sm = *reinterpret_cast<CsmTables*>(sb + kOffTables);
     int32_t* const ones = reinterpret_cast<int32_t*>(sb + kOffOnes);
     PfBars& br = *reinterpret_cast<PfBars*>(sb + kOffBars);
