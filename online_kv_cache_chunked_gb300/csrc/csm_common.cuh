@@ -35,6 +35,7 @@ struct CsmParams {
     int32_t BH, h_kv, cap, D, n1, n2, c, m, maxch, L;
     int64_t timeout_ns;
     int32_t withhold;
+    int32_t paged_tma;  // block-table layout: chunk rows by TMA in 16-row groups (n1 a multiple of 16)
 };
 
 template <typename T>

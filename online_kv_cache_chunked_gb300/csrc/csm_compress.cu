@@ -290,6 +290,7 @@ static int compress_impl(void* K, void* V, int32_t* N, int32_t* len, const csmkv
     P.maxch = maxch;
     P.L = L;
     P.rm = row_map(cache, pages);
+    P.paged_tma = (pages && n1 % 16 == 0) ? 1 : 0;  // 16-row groups then never straddle a page
     P.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : 2000000000LL;
     P.withhold = opts ? opts->withhold_signals : 0;
 

@@ -20,8 +20,10 @@
 // In-place safety: every item publishes an epoch-tagged "loaded" flag per array
 // once its TMA lands; an item writes an array only after the items whose source
 // rows it overwrites have published (see csm_compress.cu).
-// PAGED (block-table layout): a chunk's rows are gathered row by row through the
-// unit's block table with 16-byte cp.async into the same swizzled operand layout,
+// PAGED (block-table layout): a chunk's rows come through the unit's block table --
+// when n1 is a multiple of 16, by TMA in 16-row groups (each inside one page) through
+// the pool's parity view; otherwise row by row with 16-byte cp.async -- into the
+// same swizzled operand layout,
 // and every output row is stored through the table; the flags and the order of
 // the in-place writes are those of the dense layout, in logical rows.
 #include "csm_common.cuh"
@@ -253,6 +255,36 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
         }
         if (with_degrees) cp_async4(nbuf + q, p.N + pr);
     };
+    // PAGED, n1 a multiple of 16: the chunk's rows from logical row base as 16 groups of
+    // 16 rows, each inside one page, by TMA through the 3-D parity view of the pool (a
+    // box of 8 rows of one parity): lane 2 g + op loads group g's A (op 0) or B rows into
+    // rows 8 g .. 8 g + 7 of that operand's boxes. A block-table entry outside the pool
+    // gets an out-of-range coordinate (zeros land) and CSMKV_ERR_ARG. Completes on st.bar.
+    auto tma_gather_slot = [&](const CUtensorMap* map, int u, int base) {  // warp 0
+        if (lane == 0) {
+            mbar_expect_tx(&st.bar, (uint32_t)R::kSlotBytes);
+            load_pend = true;
+        }
+        __syncwarp();
+        const int g = lane >> 1, op = lane & 1;
+        const long long pr = map_row(p.rm, u, base + 16 * g);
+        int y = 0, z = -16;
+        if (pr < 0) {
+            record_status(status, CSMKV_ERR_ARG);
+        } else {
+            y = (int)((pr + op) & 1);
+            z = (int)((pr + op) >> 1);
+        }
+#pragma unroll
+        for (int bx = 0; bx < R::kBoxes; ++bx)
+            tma_load_3d(slot + (op * R::kBoxes + bx) * 16384 + g * 1024, map, &st.bar, bx * 64, y, z);
+    };
+    // PAGED: the degrees of the chunk's rows, one per thread, by cp.async (completed by
+    // cp_async_wait_all).
+    auto gather_degrees = [&](int u, int base) {  // all threads
+        const long long pr = map_row(p.rm, u, base + tid);
+        if (pr < 0) nbuf[tid] = 0; else cp_async4(nbuf + tid, p.N + pr);
+    };
     // PAGED: the 128 B rows of the slot (the output when every A row merges) stored
     // through the block table to logical rows drow .. drow + 127.
     auto store_b_rows_paged = [&](T* arr, int u, int drow) {  // all threads
@@ -288,7 +320,14 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
         const int lev = t / BH, u = t - lev * BH;
         bool ok = true;
         if constexpr (PAGED) {
-            if (lev < levels_ch) gather_slot(Kg, u, p.n1 + lev * c, true);
+            if (lev < levels_ch) {
+                if (p.paged_tma) {
+                    gather_degrees(u, p.n1 + lev * c);
+                    if (warp == 0) tma_gather_slot(&tmK, u, p.n1 + lev * c);
+                } else {
+                    gather_slot(Kg, u, p.n1 + lev * c, true);
+                }
+            }
         }
 
         if (lev < levels_ch) {
@@ -319,6 +358,10 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             if constexpr (PAGED) {
                 cp_async_wait_all();
                 fence_proxy_async_smem();  // the gathered operands before the MMA reads them
+                if (p.paged_tma) {
+                    ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
+                    phase ^= 1u;
+                }
             } else {
                 ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
                 phase ^= 1u;
@@ -450,8 +493,14 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             fence_proxy_async_smem();
             __syncthreads();
             if constexpr (PAGED) {
-                gather_slot(Vg, u, p.n1 + j * c, false);
-                cp_async_wait_all();
+                if (p.paged_tma) {
+                    if (warp == 0) tma_gather_slot(&tmV, u, p.n1 + j * c);
+                    ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
+                    phase ^= 1u;
+                } else {
+                    gather_slot(Vg, u, p.n1 + j * c, false);
+                    cp_async_wait_all();
+                }
             } else {
                 if (tid == 0) {
                     if (stores_pend) {
@@ -513,7 +562,7 @@ int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint
     CUtensorMap tmK{}, tmV{}, tmN{}, tmKs{}, tmVs{};
     const uint64_t dims[3] = {(uint64_t)D, 2, rows / 2};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
-    const uint32_t box[3] = {64, 1, 128};
+    const uint32_t box[3] = {64, 1, paged ? 8u : 128u};  // paged: 16-row groups, 8 rows of one parity
     const uint64_t ndims[2] = {4, rows / 4};
     const uint64_t nstr[1] = {16};
     const uint32_t nbox[2] = {4, (uint32_t)Tc3<128>::kNRows};

@@ -42,9 +42,11 @@ def _assert_same_cache(kv, K, V, N, L):
             assert torch.equal(N2[b, h, :s], N[b, h, :s]), (b, h)
 
 
-@pytest.mark.parametrize("page_rows,D", [(256, 128), (64, 128), (512, 64)])
-def test_paged_rounds_equal_dense_rounds_and_the_oracle(cuda_lib, page_rows, D):
-    n1, n2, c = 16, 64, 256
+@pytest.mark.parametrize("page_rows,D,n1", [(256, 128, 16), (64, 128, 16), (512, 64, 16), (64, 128, 48),
+                                             (256, 128, 10)])
+def test_paged_rounds_equal_dense_rounds_and_the_oracle(cuda_lib, page_rows, D, n1):
+    """n1 a multiple of 16: chunk rows by TMA in 16-row page groups; n1 = 10: row gathers."""
+    n2, c = 64, 256
     lengths = [[80 + 5 * 256 + 17, 80 + 3 * 256, 79, 2040], [80 + 256 + 255, 1800, 80 + 256, 0]]
     K, V, N, L = _dense_case(page_rows + D, 2, 4, 2048, D, lengths)
     kv = paged.to_paged(K, V, N, page_rows, spare_pages=7, seed=page_rows)
