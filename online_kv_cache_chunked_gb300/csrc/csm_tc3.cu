@@ -279,6 +279,24 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
         for (int bx = 0; bx < R::kBoxes; ++bx)
             tma_load_3d(slot + (op * R::kBoxes + bx) * 16384 + g * 1024, map, &st.bar, bx * 64, y, z);
     };
+    // PAGED, n1 a multiple of 16: the 128 output rows held in the B boxes (every A row
+    // merged) stored by TMA in 16-row groups through the table to logical rows drow ..
+    // drow + 127 (drow is then a multiple of 16: no group straddles a page); a group
+    // whose entry lies outside the pool is not stored and CSMKV_ERR_ARG is recorded.
+    auto store_b_rows_paged_tma = [&](const CUtensorMap* map, int u, int drow) {  // thread 0
+        for (int g = 0; g < 8; ++g) {
+            const long long pr = map_row(p.rm, u, drow + 16 * g);
+            if (pr < 0) {
+                record_status(status, CSMKV_ERR_ARG);
+                continue;
+            }
+#pragma unroll
+            for (int bx = 0; bx < R::kBoxes; ++bx)
+                tma_store_2d(map, slot + (R::kBoxes + bx) * 16384 + g * 2048, bx * 64, (int)pr);
+        }
+        bulk_commit();
+        stores_pend = true;
+    };
     // PAGED: the degrees of the chunk's rows, one per thread, by cp.async (completed by
     // cp_async_wait_all).
     auto gather_degrees = [&](int u, int base) {  // all threads
@@ -463,8 +481,14 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             if (all) {
                 merge_inplace(sN);
                 if constexpr (PAGED) {
-                    __syncthreads();
-                    store_b_rows_paged(Kg, u, dst_row);
+                    if (p.paged_tma) {
+                        fence_proxy_async_smem();
+                        __syncthreads();
+                        if (tid == 0) store_b_rows_paged_tma(&tmKs, u, dst_row);
+                    } else {
+                        __syncthreads();
+                        store_b_rows_paged(Kg, u, dst_row);
+                    }
                 } else {
                     fence_proxy_async_smem();
                     __syncthreads();
@@ -494,7 +518,14 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             __syncthreads();
             if constexpr (PAGED) {
                 if (p.paged_tma) {
-                    if (warp == 0) tma_gather_slot(&tmV, u, p.n1 + j * c);
+                    if (warp == 0) {
+                        if (tid == 0 && stores_pend) {  // the K rows' stores have left the slot
+                            bulk_wait_read_all();
+                            stores_pend = false;
+                        }
+                        __syncwarp();
+                        tma_gather_slot(&tmV, u, p.n1 + j * c);
+                    }
                     ok = mbar_wait(&st.bar, phase, globaltimer() + p.timeout_ns);
                     phase ^= 1u;
                 } else {
@@ -522,8 +553,14 @@ __global__ void __launch_bounds__(kTc3Threads, 3)
             if (all) {
                 merge_inplace(sN);
                 if constexpr (PAGED) {
-                    __syncthreads();
-                    store_b_rows_paged(Vg, u, dst_row);
+                    if (p.paged_tma) {
+                        fence_proxy_async_smem();
+                        __syncthreads();
+                        if (tid == 0) store_b_rows_paged_tma(&tmVs, u, dst_row);
+                    } else {
+                        __syncthreads();
+                        store_b_rows_paged(Vg, u, dst_row);
+                    }
                 } else {
                     fence_proxy_async_smem();
                     __syncthreads();
@@ -568,7 +605,7 @@ int launch_csm_tc3(const CsmParams& P, int D, void* K, void* V, int32_t* N, uint
     const uint32_t nbox[2] = {4, (uint32_t)Tc3<128>::kNRows};
     const uint64_t sdims[2] = {(uint64_t)D, rows};
     const uint64_t sstr[1] = {(uint64_t)D * 2};
-    const uint32_t sbox[2] = {64, 128};
+    const uint32_t sbox[2] = {64, paged ? 16u : 128u};  // paged: 16-row groups
     if (!encode_tiled(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled(&tmN, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, N, ndims, nstr, nbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
