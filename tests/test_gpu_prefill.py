@@ -155,3 +155,41 @@ def test_empty_prompt_writes_only_lengths():
     torch.cuda.synchronize()
     assert (Lo == 0).all()
     assert (out == SENTINEL).all()
+
+
+def test_full_size_prompt_sampled_rows():
+    """One layer of the 64K workload's shape in the bench's launch configuration (one
+    65536-row prompt, 32 query / 8 KV heads, fused first round r = 0.5): sampled output rows
+    of every query head against the oracle (prompt rows of the sampled positions only), and
+    the whole second cache byte-equal to the standalone round."""
+    n, h_kv, G = 65536, 8, 4
+    g = torch.Generator(device="cuda").manual_seed(2024)
+    q = torch.randn(1, h_kv * G, n, D, device="cuda", generator=g).to(torch.bfloat16)
+    K = torch.randn(1, h_kv, n + 64, D, device="cuda", generator=g).to(torch.bfloat16)
+    V = torch.randn(1, h_kv, n + 64, D, device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    Ko, Vo = torch.empty_like(K), torch.empty_like(V)
+    No = torch.empty(1, h_kv, n + 64, dtype=torch.int32, device="cuda")
+    Lo = torch.empty(1, h_kv, dtype=torch.int32, device="cuda")
+    ws = B.new_workspace(B.prefill_workspace_bytes(), "cuda")
+    B.prefill_attn_csm(q, K, V, n, out, Ko, Vo, No, Lo, 16, 64, 256, 0.5, ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0
+    rows = np.array([0, 1, 15, 16, 127, 128, 4095, 32767, 40000, n - 2, n - 1], np.int32)
+    Kc, Vc = to64(K[:, :, :n]), to64(V[:, :, :n])
+    for h in range(0, h_kv * G, 5):  # a spread of query heads (every KV head is read by one)
+        ref = oracle.prefill_attn(to64(q[:, h:h + 1]), Kc[:, h // G:h // G + 1], Vc[:, h // G:h // G + 1], n, 1,
+                                  rows=rows)
+        got = to64(out[:, h:h + 1, rows])
+        err = float(np.abs(got - ref).max())
+        assert err <= compare.ATTN_TOL["bf16"], f"head {h}: attention max error {err}"
+    Ks, Vs = K.clone(), V.clone()
+    Ns = torch.ones(1, h_kv, n + 64, dtype=torch.int32, device="cuda")
+    Ls = torch.full((1, h_kv), n, dtype=torch.int32, device="cuda")
+    wsc = B.new_workspace(B.csm_workspace_bytes(B.cache_desc(Ks), 16, 64, 256), "cuda")
+    B.csm_compress(Ks, Vs, Ns, Ls, 16, 64, 256, 0.5, workspace=wsc)
+    torch.cuda.synchronize()
+    assert torch.equal(Lo, Ls)
+    s = int(Ls[0, 0])
+    assert torch.equal(Ko[:, :, :s], Ks[:, :, :s]) and torch.equal(Vo[:, :, :s], Vs[:, :, :s])
+    assert torch.equal(No[:, :, :s], Ns[:, :, :s])
