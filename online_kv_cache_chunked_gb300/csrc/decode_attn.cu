@@ -51,7 +51,11 @@ constexpr int kUnitBits = 9;           // scan tables pack (len << kUnitBits) | 
 #define CSMKV_DEC_MAX_SPLITS 64
 #endif
 constexpr int kItemsPerCta = CSMKV_DEC_ITEMS;           // splits per equal share of the GPU
-constexpr int kMinSplit = 256;                          // tokens (4 tiles: per-split costs stay small)
+#ifndef CSMKV_DEC_MIN_SPLIT
+#define CSMKV_DEC_MIN_SPLIT 256
+#endif
+constexpr int kMinSplit = CSMKV_DEC_MIN_SPLIT;          // tokens (4 tiles: per-split costs stay small)
+static_assert(kMinSplit % 64 == 0 && kMinSplit > 0, "the minimum split is a whole number of tiles");
 constexpr int kMaxSplitsPerUnit = CSMKV_DEC_MAX_SPLITS;  // bounds the records one unit's merge reads
 constexpr uint32_t kFirst = 1u, kLast = 2u;
 constexpr int kSlotHeads = 8;          // query heads of a group the MMA covers (N = 8)
