@@ -57,6 +57,16 @@ constexpr int kItemsPerCta = CSMKV_DEC_ITEMS;           // splits per equal shar
 constexpr int kMinSplit = CSMKV_DEC_MIN_SPLIT;          // tokens (4 tiles: per-split costs stay small)
 static_assert(kMinSplit % 64 == 0 && kMinSplit > 0, "the minimum split is a whole number of tiles");
 constexpr int kMaxSplitsPerUnit = CSMKV_DEC_MAX_SPLITS;  // bounds the records one unit's merge reads
+#ifndef CSMKV_DEC_PREFETCH_DIV
+#define CSMKV_DEC_PREFETCH_DIV 4
+#endif
+#ifndef CSMKV_DEC_PREFETCH_MAX
+#define CSMKV_DEC_PREFETCH_MAX 1024
+#endif
+// rows a CTA pulls into L2 while the call is planned: 1/kPrefetchDiv of its share
+// of the call, in [64, kPrefetchMax] (0: none)
+constexpr int kPrefetchDiv = CSMKV_DEC_PREFETCH_DIV;
+constexpr int kPrefetchMax = CSMKV_DEC_PREFETCH_MAX;
 constexpr uint32_t kFirst = 1u, kLast = 2u;
 constexpr int kSlotHeads = 8;          // query heads of a group the MMA covers (N = 8)
 #ifndef CSMKV_DEC_CLAIM_EARLY
@@ -447,6 +457,32 @@ __device__ __forceinline__ int plan_class(int len, int S, int total, int n) {
     return unit_class(unit_nsplit(len, su), su, S);
 }
 
+// While one warp plans the call, HBM would sit idle. Every row below a unit's
+// length is read by the call, so the producer warp of CTA b asks L2 for the first
+// rows of K and V of piece b / BH of unit b % BH (each unit's rows cut into as many
+// pieces as there are CTAs per unit): 1/kPrefetchDiv of a CTA's share of the call's
+// rows, in [64, kPrefetchMax]. The split that reads those rows later finds them in
+// L2. Dense layout only; rows[u] are the rows unit u attends.
+template <int D>
+__device__ __forceinline__ void prefetch_piece(const DecParams& p, const int* rows, int lane) {
+    long long t = 0;
+    for (int u = lane; u < p.BH; u += 32) t += rows[u];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const int b = (int)blockIdx.x, nb = (int)gridDim.x;
+    const long long share = t / ((long long)nb * kPrefetchDiv);
+    const int want = (int)min((long long)kPrefetchMax, max(64ll, share & ~63ll));
+    const int u = b % p.BH, j = b / p.BH;
+    const int pieces = (nb + p.BH - 1) / p.BH;
+    const int len = rows[u];
+    const int piece = (len + pieces - 1) / pieces;
+    const int r0 = j * piece;
+    const int nr = min(min(want, piece), len - r0);
+    if (nr <= 0 || lane > 1) return;
+    const size_t off = ((size_t)u * p.cap + r0) * D * 2;
+    bulk_prefetch_l2(static_cast<const uint8_t*>(lane ? p.V : p.K) + off, (uint32_t)nr * D * 2);
+}
+
 // SCAN: the CTA computes the unit order and split offsets itself (units <=
 // kMaxScanUnits, kept in shared memory); otherwise decode_prologue_kernel has
 // written them to the workspace.
@@ -494,6 +530,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 #pragma unroll 4
         for (int u = tid; u < p.BH; u += kDecThreads) sp[u] = eff_len(p, u, true);
         __syncthreads();
+        if (kPrefetchDiv > 0 && warp == kConsumerWarps && !p.rm.table) prefetch_piece<D>(p, sp, lane);
         if (warp == 0) {
             const int per = (p.BH + 31) / 32;
             const int ub = min(p.BH, lane * per), ue = min(p.BH, ub + per);
