@@ -462,7 +462,8 @@ __device__ __forceinline__ int plan_class(int len, int S, int total, int n) {
 // rows of K and V of piece b / BH of unit b % BH (each unit's rows cut into as many
 // pieces as there are CTAs per unit): 1/kPrefetchDiv of a CTA's share of the call's
 // rows, in [64, kPrefetchMax]. The split that reads those rows later finds them in
-// L2. Dense layout only; rows[u] are the rows unit u attends.
+// L2. rows[u] are the rows unit u attends. Paged layout: one prefetch per page the
+// rows touch, lanes over the pages; a table entry outside the pool is skipped.
 template <int D>
 __device__ __forceinline__ void prefetch_piece(const DecParams& p, const int* rows, int lane) {
     long long t = 0;
@@ -478,9 +479,23 @@ __device__ __forceinline__ void prefetch_piece(const DecParams& p, const int* ro
     const int piece = (len + pieces - 1) / pieces;
     const int r0 = j * piece;
     const int nr = min(min(want, piece), len - r0);
-    if (nr <= 0 || lane > 1) return;
-    const size_t off = ((size_t)u * p.cap + r0) * D * 2;
-    bulk_prefetch_l2(static_cast<const uint8_t*>(lane ? p.V : p.K) + off, (uint32_t)nr * D * 2);
+    if (nr <= 0) return;
+    constexpr int kRowBytes = D * 2;
+    if (!p.rm.table) {
+        if (lane > 1) return;
+        const size_t off = ((size_t)u * p.cap + r0) * kRowBytes;
+        bulk_prefetch_l2(static_cast<const uint8_t*>(lane ? p.V : p.K) + off, (uint32_t)nr * kRowBytes);
+        return;
+    }
+    const int P = p.rm.P, pg0 = r0 / P, pg1 = (r0 + nr - 1) / P;
+    for (int pi = pg0 + lane; pi <= pg1 && pi < p.rm.maxp; pi += 32) {
+        const int pg = __ldg(p.rm.table + (size_t)u * p.rm.maxp + pi);
+        if (pg < 0 || pg >= p.rm.npages) continue;
+        const int a = max(r0, pi * P), e = min(r0 + nr, (pi + 1) * P);
+        const size_t off = ((size_t)pg * P + (a - pi * P)) * kRowBytes;
+        bulk_prefetch_l2(static_cast<const uint8_t*>(p.K) + off, (uint32_t)(e - a) * kRowBytes);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(p.V) + off, (uint32_t)(e - a) * kRowBytes);
+    }
 }
 
 // SCAN: the CTA computes the unit order and split offsets itself (units <=
@@ -530,7 +545,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 #pragma unroll 4
         for (int u = tid; u < p.BH; u += kDecThreads) sp[u] = eff_len(p, u, true);
         __syncthreads();
-        if (kPrefetchDiv > 0 && warp == kConsumerWarps && !p.rm.table) prefetch_piece<D>(p, sp, lane);
+        if (kPrefetchDiv > 0 && warp == kConsumerWarps) prefetch_piece<D>(p, sp, lane);
         if (warp == 0) {
             const int per = (p.BH + 31) / 32;
             const int ub = min(p.BH, lane * per), ue = min(p.BH, ub + per);
