@@ -450,12 +450,8 @@ __device__ __forceinline__ int warp_excl(int v) {
     }
     return incl - v;
 }
-// Ticket-order class of a unit of `len` rows (empty units last).
-__device__ __forceinline__ int plan_class(int len, int S, int total, int n) {
-    if (len <= 0) return 3;
-    const int su = unit_split(len, S, total, n);
-    return unit_class(unit_nsplit(len, su), su, S);
-}
+// The plan's per-unit scratch lives in the merge scratch's accumulator rows.
+static_assert(kMaxScanUnits <= kSlotHeads * kRedStride, "one int per unit fits the merge scratch");
 
 // While one warp plans the call, HBM would sit idle. Every row below a unit's
 // length is read by the call, so the producer warp of CTA b asks L2 for the first
@@ -554,12 +550,23 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             for (int u = ub; u < ue; ++u) total += sp[u];
             total = warp_sum(total);
             const int S = split_base(total, (int)gridDim.x);
+            // every unit's split count and class, computed once (the divisions are the
+            // bulk of this code, fetched cold) and kept in the merge scratch, which is
+            // first written at the end of a split: nsc[u] = splits << 2 | class
+            int* const nsc = reinterpret_cast<int*>(&sm.cs.acc[0][0]);
             // positions: classes in order, units in index order inside a class; the
             // four class counts (each <= kMaxScanUnits < 2^16) travel packed in two ints
             int c01 = 0, c23 = 0;
 #pragma unroll 1
             for (int u = ub; u < ue; ++u) {
-                const int cls = plan_class(sp[u], S, total, p.nCTA);
+                const int len = sp[u];
+                int ns = 0, cls = 3;
+                if (len > 0) {
+                    const int su = unit_split(len, S, total, p.nCTA);
+                    ns = unit_nsplit(len, su);
+                    cls = unit_class(ns, su, S);
+                }
+                nsc[u] = (ns << 2) | cls;
                 c01 += cls == 0 ? 1 : (cls == 1 ? 0x10000 : 0);
                 c23 += cls == 2 ? 1 : (cls == 3 ? 0x10000 : 0);
             }
@@ -571,27 +578,24 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
             int pos3 = (t01 & 0xFFFF) + (t01 >> 16) + (t23 & 0xFFFF) + (e23 >> 16);
 #pragma unroll 1
             for (int u = ub; u < ue; ++u) {
-                const int cls = plan_class(sp[u], S, total, p.nCTA);
+                const int cls = nsc[u] & 3;
                 const int pos = cls == 0 ? pos0++ : (cls == 1 ? pos1++ : (cls == 2 ? pos2++ : pos3++));
                 ulen[pos] = ((uint32_t)sp[u] << kUnitBits) | (uint32_t)u;
             }
             __syncwarp();
             // in ticket order: every position's splits and its first split
+            constexpr uint32_t kUnitMask = (1u << kUnitBits) - 1u;
             int ns = 0;
 #pragma unroll 1
-            for (int q = ub; q < ue; ++q) {
-                const int len = (int)(ulen[q] >> kUnitBits);
-                ns += len > 0 ? unit_nsplit(len, unit_split(len, S, total, p.nCTA)) : 0;
-            }
+            for (int q = ub; q < ue; ++q) ns += nsc[ulen[q] & kUnitMask] >> 2;
             int first = warp_excl(ns);
             const int nsplits_all = __shfl_sync(0xffffffffu, first + ns, 31);
 #pragma unroll 1
             for (int q = ub; q < ue; ++q) {
-                const int len = (int)(ulen[q] >> kUnitBits);
-                const int n = len > 0 ? unit_nsplit(len, unit_split(len, S, total, p.nCTA)) : 0;
+                const int u = (int)(ulen[q] & kUnitMask);
+                const int n = nsc[u] >> 2;
                 sp[q] = first;
                 if (blockIdx.x == 0) {  // for the merge kernel
-                    const int u = (int)(ulen[q] & ((1u << kUnitBits) - 1u));
                     p.g_first[u] = first;
                     p.g_n[u] = n;
                 }
