@@ -714,20 +714,55 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     hN.copy_(N0)
     hL.copy_(L0)
     pre = [rd for rd in rounds if rd.step == 0]
-    s_after = pre[-1].s_after[0] if pre else w.n[0]
     BH = w.batch * w.h_kv
-    oK = torch.empty((BH, s_after, w.d), dtype=K0.dtype).pin_memory()
-    oV = torch.empty((BH, s_after, w.d), dtype=V0.dtype).pin_memory()
-    oN = torch.empty((BH, s_after), dtype=torch.int32).pin_memory()
+    # rows every cache holds after the prefill round(s): its sequence's compressed
+    # length, or the prompt length for a KV head the mask leaves out
+    comp0 = np.array(w.n, np.int64)
+    for rd in pre:
+        for i, sa in zip(rd.seqs, rd.s_after):
+            comp0[i] = sa
+    hmask = d["head_mask"].cpu().numpy().astype(bool)
+    fin = np.array([np.where(hmask, w.n[b % w.seqs], comp0[b % w.seqs]) for b in range(w.batch)], np.int64)
     stream = torch.cuda.current_stream()
     tokens = sum(csm_call_stats(w, rd, d["head_mask"].cpu().numpy())[0] for rd in pre)
-    # Pipelined by groups of cache rows (layers x sequences): group g's upload, its
-    # prefill round(s) and its download run on three streams, so one group's
-    # transfers overlap another's compression and the two copy directions overlap
-    # (a second upload stream was slower: the uploads share the host link). Smaller
-    # groups shorten the download of the last group, which nothing overlaps.
-    G = max(1, min(args.e2e_groups, w.batch))
-    bounds = [(g * w.batch // G, (g + 1) * w.batch // G) for g in range(G)]
+    # Pipelined by groups of caches: group g's upload, its prefill round(s) and its
+    # download run on three streams, so one group's transfers overlap another's
+    # compression and the two copy directions overlap (a second upload stream was
+    # slower: the uploads share the host link). Smaller groups shorten the download
+    # of the last group, which nothing overlaps. A group is a range of cache rows
+    # (layers x sequences) with all their KV heads or, when there are fewer rows
+    # than groups wanted, one row's range of KV heads (every (row, KV head) cache is
+    # compressed on its own, and such a slice is contiguous). Every group costs the
+    # host about a dozen copy and launch calls (~0.1 ms), so a group uploads at
+    # least 64 MB (measured: 32K x 4 best at 8 groups of 70 MB, 0.81 of the link,
+    # 0.67 at 16 groups).
+    h2d_all = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
+    want = max(1, min(args.e2e_groups, h2d_all // (64 << 20)))
+    if w.batch >= want:
+        bounds = [(g * w.batch // want, (g + 1) * w.batch // want, 0, w.h_kv) for g in range(want)]
+    else:
+        hs = min(w.h_kv, -(-want // w.batch))
+        bounds = [(b, b + 1, j * w.h_kv // hs, (j + 1) * w.h_kv // hs) for b in range(w.batch) for j in range(hs)]
+    G = len(bounds)
+    # each group's download: runs of consecutive caches of one row with the same
+    # length, every run into its own contiguous stretch of the host buffers
+    runs = []  # (group, first unit, end unit, rows, offset in rows)
+    off = 0
+    for g, (b0, b1, h0, h1) in enumerate(bounds):
+        for b in range(b0, b1):
+            h = h0
+            while h < h1:
+                e = h + 1
+                while e < h1 and fin[b, e] == fin[b, h]:
+                    e += 1
+                L = int(fin[b, h])
+                runs.append((g, b * w.h_kv + h, b * w.h_kv + e, L, off))
+                off += (e - h) * L
+                h = e
+    oK = torch.empty((off, w.d), dtype=K0.dtype).pin_memory()
+    oV = torch.empty((off, w.d), dtype=V0.dtype).pin_memory()
+    oN = torch.empty((off,), dtype=torch.int32).pin_memory()
+    dK, dV, dN = d["K"].view(BH, -1, w.d), d["V"].view(BH, -1, w.d), d["N"].view(BH, -1)
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     pre_k = [k for k, rd in enumerate(rounds) if rd.step == 0]
     times = []
@@ -736,28 +771,31 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
         e0.record(stream)
         for st_ in (s_in, s_cmp, s_out):
             st_.wait_event(e0)
-        for b0, b1 in bounds:
+        for g, (b0, b1, h0, h1) in enumerate(bounds):
             ev_in, ev_c = torch.cuda.Event(), torch.cuda.Event()
             with torch.cuda.stream(s_in):
                 for key, host in (("K", hK), ("V", hV), ("N", hN), ("len", hL)):
-                    d[key][b0:b1].copy_(host[b0:b1], non_blocking=True)
+                    d[key][b0:b1, h0:h1].copy_(host[b0:b1, h0:h1], non_blocking=True)
                 ev_in.record(s_in)
             s_cmp.wait_event(ev_in)
             for k in pre_k:
                 rd = rounds[k]
                 mask = p.masks[k]
                 lim = p.limits[k]
-                B.csm_compress_ex(d["K"][b0:b1], d["V"][b0:b1], d["N"][b0:b1], d["len"][b0:b1], w.n1, w.n2, w.c,
-                                  rd.r, p.head_mask, None if mask is None else mask[b0:b1],
+                B.csm_compress_ex(d["K"][b0:b1, h0:h1], d["V"][b0:b1, h0:h1], d["N"][b0:b1, h0:h1],
+                                  d["len"][b0:b1, h0:h1], w.n1, w.n2, w.c, rd.r,
+                                  None if p.head_mask is None else p.head_mask[h0:h1],
+                                  None if mask is None else mask[b0:b1],
                                   seq_max_chunks=None if lim is None else lim[b0:b1], workspace=p.ws_csm,
                                   stream=s_cmp)
             ev_c.record(s_cmp)
             s_out.wait_event(ev_c)
-            u0, u1 = b0 * w.h_kv, b1 * w.h_kv
             with torch.cuda.stream(s_out):
-                oK[u0:u1].copy_(d["K"].view(BH, -1, w.d)[u0:u1, :s_after], non_blocking=True)
-                oV[u0:u1].copy_(d["V"].view(BH, -1, w.d)[u0:u1, :s_after], non_blocking=True)
-                oN[u0:u1].copy_(d["N"].view(BH, -1)[u0:u1, :s_after], non_blocking=True)
+                for _, u0, u1, L, o in (r_ for r_ in runs if r_[0] == g):
+                    n_ = (u1 - u0) * L
+                    oK[o:o + n_].view(u1 - u0, L, w.d).copy_(dK[u0:u1, :L], non_blocking=True)
+                    oV[o:o + n_].view(u1 - u0, L, w.d).copy_(dV[u0:u1, :L], non_blocking=True)
+                    oN[o:o + n_].view(u1 - u0, L).copy_(dN[u0:u1, :L], non_blocking=True)
         stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -766,6 +804,26 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
     d2h = sum(t.numel() * t.element_size() for t in (oK, oV, oN))
     t_e2e = float(np.median(times))
+    # untimed: the grouped result equals one call over the whole cache, byte for byte
+    for key, src in (("K", K0), ("V", V0), ("N", N0), ("len", L0)):
+        d[key].copy_(src)
+    for k in pre_k:
+        mask, lim = p.masks[k], p.limits[k]
+        B.csm_compress_ex(d["K"], d["V"], d["N"], d["len"], w.n1, w.n2, w.c, rounds[k].r, p.head_mask, mask,
+                          seq_max_chunks=lim, workspace=p.ws_csm)
+    torch.cuda.synchronize()
+    if not np.array_equal(d["len"].cpu().numpy(), fin):
+        raise RuntimeError("end-to-end leg: lengths after the prefill round disagree with the host schedule")
+    def bits(t):
+        return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+    for _, u0, u1, L, o in runs:
+        n_ = (u1 - u0) * L
+        same = (torch.equal(bits(oK[o:o + n_].view(u1 - u0, L, w.d)), bits(dK[u0:u1, :L].cpu()))
+                and torch.equal(bits(oV[o:o + n_].view(u1 - u0, L, w.d)), bits(dV[u0:u1, :L].cpu()))
+                and torch.equal(oN[o:o + n_].view(u1 - u0, L), dN[u0:u1, :L].cpu()))
+        if not same:
+            raise RuntimeError(f"end-to-end leg: caches {u0}..{u1 - 1} differ from one call over the whole cache")
     link = host_link()
     # attention decode steps from host buffers: H2D of q, k, v; append; attend; D2H of o
     nsteps = min(50, w.steps)
@@ -794,7 +852,7 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     bound = max(h2d / link["h2d_gbs"], (h2d + d2h) / link["both_gbs"]) / 1e9
     return {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
-            f"compress, D2H compacted rows, pipelined over {G} groups of cache rows",
+            f"compress, D2H compacted rows, pipelined over {G} groups of caches",
             "ms": t_e2e * 1e3, "h2d_gbs": h2d / t_e2e / 1e9, "host_link_gbs": (h2d + d2h) / t_e2e / 1e9,
             "link": link, "link_bound_ms": bound * 1e3, "link_frac": bound / t_e2e,
             "decode_attn_gbs_at_prefill_round_length": step_bytes * nsteps / att_s / 1e9,
