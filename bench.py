@@ -732,12 +732,14 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     # of the last group, which nothing overlaps. A group is a range of cache rows
     # (layers x sequences) with all their KV heads or, when there are fewer rows
     # than groups wanted, one row's range of KV heads (every (row, KV head) cache is
-    # compressed on its own, and such a slice is contiguous). Every group costs the
-    # host about a dozen copy and launch calls (~0.1 ms), so a group uploads at
-    # least 64 MB (measured: 32K x 4 best at 8 groups of 70 MB, 0.81 of the link,
-    # 0.67 at 16 groups).
+    # compressed on its own, and such a slice is contiguous). A group costs a dozen
+    # copies and two kernels: groups upload at least 64 MB, but there are at least 8
+    # when the iteration runs as a CUDA graph (below) -- the host then no longer
+    # issues every call (measured: 32K x 4 best at 8 groups of 70 MB, 0.82 of the
+    # link, 0.77 at 32; the 16K layer 0.62 at 8 groups of 9 MB, 0.52 at one).
     h2d_all = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
-    want = max(1, min(args.e2e_groups, h2d_all // (64 << 20)))
+    want = max(0 if args.e2e_eager else 8, h2d_all // (64 << 20))
+    want = max(1, min(args.e2e_groups, want))
     if w.batch >= want:
         bounds = [(g * w.batch // want, (g + 1) * w.batch // want, 0, w.h_kv) for g in range(want)]
     else:
@@ -765,12 +767,15 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     dK, dV, dN = d["K"].view(BH, -1, w.d), d["V"].view(BH, -1, w.d), d["N"].view(BH, -1)
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     pre_k = [k for k, rd in enumerate(rounds) if rd.step == 0]
-    times = []
-    for it in range(args.warmup + max(1, args.steps)):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+
+    def issue():
+        """One iteration: every group's upload, prefill round(s) and download, forked
+        from the current stream onto the three streams and joined back into it."""
+        cur = torch.cuda.current_stream()
+        ev0 = torch.cuda.Event()
+        ev0.record(cur)
         for st_ in (s_in, s_cmp, s_out):
-            st_.wait_event(e0)
+            st_.wait_event(ev0)
         for g, (b0, b1, h0, h1) in enumerate(bounds):
             ev_in, ev_c = torch.cuda.Event(), torch.cuda.Event()
             with torch.cuda.stream(s_in):
@@ -796,7 +801,34 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
                     oK[o:o + n_].view(u1 - u0, L, w.d).copy_(dK[u0:u1, :L], non_blocking=True)
                     oV[o:o + n_].view(u1 - u0, L, w.d).copy_(dV[u0:u1, :L], non_blocking=True)
                     oN[o:o + n_].view(u1 - u0, L).copy_(dN[u0:u1, :L], non_blocking=True)
-        stream.wait_stream(s_out)
+        for st_ in (s_in, s_cmp, s_out):
+            cur.wait_stream(st_)
+
+    # The iteration is captured once in a CUDA graph and replayed: every replay
+    # still uploads, compresses and downloads every group, without the host's
+    # per-call cost (a dozen copy and launch calls per group). Eager issue if the
+    # capture fails.
+    graph = None
+    if not args.e2e_eager:
+        try:
+            issue()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+                issue()
+            torch.cuda.synchronize()
+        except RuntimeError as exc:
+            print(f"e2e: CUDA graph capture failed ({exc}); issuing eagerly", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+    times = []
+    for it in range(args.warmup + max(1, args.steps)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            issue()
         e1.record(stream)
         torch.cuda.synchronize()
         if it >= args.warmup:
@@ -852,7 +884,8 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     bound = max(h2d / link["h2d_gbs"], (h2d + d2h) / link["both_gbs"]) / 1e9
     return {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "what": "prefill CSM round from pinned host buffers: H2D cache, "
-            f"compress, D2H compacted rows, pipelined over {G} groups of caches",
+            f"compress, D2H compacted rows, pipelined over {G} groups of caches"
+            + (", one CUDA graph replayed per iteration" if graph is not None else ", issued eagerly"),
             "ms": t_e2e * 1e3, "h2d_gbs": h2d / t_e2e / 1e9, "host_link_gbs": (h2d + d2h) / t_e2e / 1e9,
             "link": link, "link_bound_ms": bound * 1e3, "link_frac": bound / t_e2e,
             "decode_attn_gbs_at_prefill_round_length": step_bytes * nsteps / att_s / 1e9,
@@ -883,6 +916,8 @@ def main():
     ap.add_argument("--page-rows", type=int, default=256)
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the fused prefill attention + first round leg")
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="issue the end-to-end leg's copies and calls from the host every iteration (no CUDA graph)")
     ap.add_argument("--e2e-groups", type=int, default=32,
                     help="the end-to-end leg pipelines uploads, compression and downloads over this many "
                          "groups of cache rows")
