@@ -297,3 +297,32 @@ def test_many_short_units(cuda_lib, kernel):
             r = ref[name][0, :got]
             assert np.all(np.abs(r - to64(T[u, :got])) <= compare.value_tol(r, "bf16", src[0, :s]))
     log_near_ties(log, f"many short units kernel={kernel}")
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_head_slices_match_whole_cache(cuda_lib, D):
+    """A range of one sequence row's KV heads, passed as its own cache (a contiguous
+    [1, heads, cap, d] view), compresses to the same bytes as one call over the whole
+    cache: every (sequence, KV head) cache is a separate unit ([Chelsea] §三 分块软匹配算法)."""
+    rng = np.random.default_rng(77 + D)
+    n1, n2, c, r = 16, 64, 256, 0.45
+    lengths = [[80 + 5 * 256 + 17, 80 + 3 * 256, 1800, 79], [80 + 256 + 255, 1800, 80 + 256, 1500]]
+    K, V, N, L = _random_cache(rng, 2, 4, 2048, D, "bf16", lengths, rho=0.93, degrees=True)
+    hm = torch.tensor([0, 1, 0, 0], dtype=torch.uint8, device="cuda")
+    sm = torch.tensor([1, 1], dtype=torch.uint8, device="cuda")
+    whole = [t.clone() for t in (K, V, N, L)]
+    ws = B.new_workspace(B.csm_workspace_bytes(B.cache_desc(K), n1, n2, c), "cuda")
+    B.csm_compress_ex(*whole, n1, n2, c, r, hm, sm, workspace=ws)
+    parts = [t.clone() for t in (K, V, N, L)]
+    for b, h0, h1 in [(0, 0, 1), (0, 1, 4), (1, 0, 2), (1, 2, 4)]:
+        Kp, Vp, Np, Lp = (t[b:b + 1, h0:h1] for t in parts)
+        B.csm_compress_ex(Kp, Vp, Np, Lp, n1, n2, c, r, hm[h0:h1], sm[b:b + 1], workspace=ws)
+    torch.cuda.synchronize()
+    assert B.csmkv_device_status(ws) == 0
+    assert torch.equal(parts[3], whole[3])
+    for b in range(2):
+        for h in range(4):
+            s = int(whole[3][b, h])
+            assert torch.equal(parts[0][b, h, :s].view(torch.int16), whole[0][b, h, :s].view(torch.int16)), (b, h)
+            assert torch.equal(parts[1][b, h, :s].view(torch.int16), whole[1][b, h, :s].view(torch.int16)), (b, h)
+            assert torch.equal(parts[2][b, h, :s], whole[2][b, h, :s]), (b, h)
