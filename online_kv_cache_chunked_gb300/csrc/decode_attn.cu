@@ -45,7 +45,7 @@ constexpr int kDecCtasPerSm = 2;
 constexpr int kMaxScanUnits = 512;     // units whose plan a CTA computes itself
 constexpr int kUnitBits = 9;           // scan tables pack (len << kUnitBits) | unit
 #ifndef CSMKV_DEC_ITEMS
-#define CSMKV_DEC_ITEMS 8
+#define CSMKV_DEC_ITEMS 6
 #endif
 #ifndef CSMKV_DEC_MAX_SPLITS
 #define CSMKV_DEC_MAX_SPLITS 64
