@@ -1,4 +1,4 @@
-"""Helpers for the GPU parity tests: run a CSM round through the C ABI and judge it
+"""Helpers for the GPU parity tests: run a CSM round through the C ABI and check it
 against the oracle with the rules in oracle/compare.py.
 
 Near-ties: every device decision that differs from the oracle's (allowed only where
