@@ -26,7 +26,9 @@
 // result does not depend on which CTA ran which split, and no merge waits on a
 // streaming CTA. The unit order and split offsets come from scans of the
 // lengths inside every CTA (batches of up to kMaxScanUnits units), or from a
-// one-CTA prologue for larger batches.
+// one-CTA prologue for larger batches; while a CTA plans, its producer warp has
+// L2 prefetch a slice of rows the call is sure to read (prefetch_piece), so HBM
+// works from the first microsecond.
 // After a device error the workspace must be zero-filled again before reuse.
 #include <cuda_bf16.h>
 
