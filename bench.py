@@ -697,6 +697,34 @@ def host_link(reps=3, nb=256 << 20):
             "both_gbs": timed(both, 2 * half), "bytes": int(nb)}
 
 
+def e2e_groups(batch, h_kv, fin, want):
+    """The end-to-end leg's groups and downloads. A group is a range of cache rows
+    with all their KV heads or, with fewer rows than `want` groups, one row's range
+    of KV heads: (row0, row1, head0, head1). Each group's download is made of runs
+    of consecutive caches of one row with the same final length fin[row, head]:
+    (group, first unit, end unit, rows, offset in rows of the host buffers), every
+    run in its own contiguous stretch. Returns (groups, runs, total rows)."""
+    if batch >= want:
+        bounds = [(g * batch // want, (g + 1) * batch // want, 0, h_kv) for g in range(want)]
+    else:
+        hs = min(h_kv, -(-want // batch))
+        bounds = [(b, b + 1, j * h_kv // hs, (j + 1) * h_kv // hs) for b in range(batch) for j in range(hs)]
+    runs = []
+    off = 0
+    for g, (b0, b1, h0, h1) in enumerate(bounds):
+        for b in range(b0, b1):
+            h = h0
+            while h < h1:
+                e = h + 1
+                while e < h1 and fin[b, e] == fin[b, h]:
+                    e += 1
+                L = int(fin[b, h])
+                runs.append((g, b * h_kv + h, b * h_kv + e, L, off))
+                off += (e - h) * L
+                h = e
+    return bounds, runs, off
+
+
 def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     """CSM end to end from pinned host buffers: H2D of the prefill cache, the prefill
     round(s), D2H of the compacted rows (pipelined over groups of layers on separate
@@ -740,27 +768,8 @@ def e2e_measure(w, d, K0, V0, N0, L0, p, rounds, args):
     h2d_all = sum(t.numel() * t.element_size() for t in (hK, hV, hN, hL))
     want = max(0 if args.e2e_eager else 8, h2d_all // (64 << 20))
     want = max(1, min(args.e2e_groups, want))
-    if w.batch >= want:
-        bounds = [(g * w.batch // want, (g + 1) * w.batch // want, 0, w.h_kv) for g in range(want)]
-    else:
-        hs = min(w.h_kv, -(-want // w.batch))
-        bounds = [(b, b + 1, j * w.h_kv // hs, (j + 1) * w.h_kv // hs) for b in range(w.batch) for j in range(hs)]
+    bounds, runs, off = e2e_groups(w.batch, w.h_kv, fin, want)
     G = len(bounds)
-    # each group's download: runs of consecutive caches of one row with the same
-    # length, every run into its own contiguous stretch of the host buffers
-    runs = []  # (group, first unit, end unit, rows, offset in rows)
-    off = 0
-    for g, (b0, b1, h0, h1) in enumerate(bounds):
-        for b in range(b0, b1):
-            h = h0
-            while h < h1:
-                e = h + 1
-                while e < h1 and fin[b, e] == fin[b, h]:
-                    e += 1
-                L = int(fin[b, h])
-                runs.append((g, b * w.h_kv + h, b * w.h_kv + e, L, off))
-                off += (e - h) * L
-                h = e
     oK = torch.empty((off, w.d), dtype=K0.dtype).pin_memory()
     oV = torch.empty((off, w.d), dtype=V0.dtype).pin_memory()
     oN = torch.empty((off,), dtype=torch.int32).pin_memory()
