@@ -50,7 +50,7 @@ constexpr int kUnitBits = 9;           // scan tables pack (len << kUnitBits) | 
 #define CSMKV_DEC_ITEMS 6
 #endif
 #ifndef CSMKV_DEC_MAX_SPLITS
-#define CSMKV_DEC_MAX_SPLITS 64
+#define CSMKV_DEC_MAX_SPLITS 40
 #endif
 constexpr int kItemsPerCta = CSMKV_DEC_ITEMS;           // splits per equal share of the GPU
 #ifndef CSMKV_DEC_MIN_SPLIT
